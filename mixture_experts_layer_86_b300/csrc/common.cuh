@@ -1,0 +1,104 @@
+// Shared device helpers of the MoE layer library (element access,
+// activations, warp reductions).  Internal header.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_b300.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Element load/store with the element type chosen at run time
+// (MOE_F32 or MOE_BF16).  Used by kernels that serve both types.
+__device__ __forceinline__ float load_elem(const void *p, int dtype, int64_t i) {
+  if (dtype == MOE_F32) return static_cast<const float *>(p)[i];
+  return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+}
+
+__device__ __forceinline__ void store_elem(void *p, int dtype, int64_t i, float v) {
+  if (dtype == MOE_F32)
+    static_cast<float *>(p)[i] = v;
+  else
+    static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+}
+
+__host__ __device__ __forceinline__ int elem_bytes(int dtype) {
+  return dtype == MOE_F32 ? 4 : 2;
+}
+
+// Activations of the expert FFN (MoE explainer §3.1 Step 4: GELU; ReLU for
+// the small fp32 layer).  tanhf / erff are CUDA's own functions.
+__device__ __forceinline__ float act_fwd(float z, int act) {
+  if (act == MOE_ACT_RELU) return fmaxf(z, 0.0f);
+  if (act == MOE_ACT_GELU_TANH) {
+    const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+    return 0.5f * z * (1.0f + tanhf(u));
+  }
+  return 0.5f * z * (1.0f + erff(z * 0.7071067811865476f));
+}
+
+// d act / d z.
+__device__ __forceinline__ float act_grad(float z, int act) {
+  if (act == MOE_ACT_RELU) return z > 0.0f ? 1.0f : 0.0f;
+  if (act == MOE_ACT_GELU_TANH) {
+    const float z2 = z * z;
+    const float u = 0.7978845608028654f * (z + 0.044715f * z2 * z);
+    const float t = tanhf(u);
+    const float du = 0.7978845608028654f * (1.0f + 0.134145f * z2);
+    return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * du;
+  }
+  const float pdf = 0.3989422804014327f * expf(-0.5f * z * z);
+  return 0.5f * (1.0f + erff(z * 0.7071067811865476f)) + z * pdf;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  return v;
+}
+
+// Arg-max over the warp with ties to the lower index; idx < 0 marks "none".
+__device__ __forceinline__ void warp_argmax(float &v, int &idx) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(kFullMask, v, o);
+    const int oi = __shfl_xor_sync(kFullMask, idx, o);
+    const bool take = (oi >= 0) && (idx < 0 || ov > v || (ov == v && oi < idx));
+    if (take) {
+      v = ov;
+      idx = oi;
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Error codes a kernel writes into the device error word (first writer
+// wins).  High byte: kernel; low bytes: the wait that gave up.
+enum : uint32_t {
+  kErrGemmProducer = 0x01000000u,
+  kErrGemmMma = 0x02000000u,
+  kErrGemmEpilogue = 0x03000000u,
+  kErrGemmDrain = 0x04000000u,
+};
+
+__device__ __forceinline__ void record_error(unsigned int *err, uint32_t code) {
+  if (err) atomicCAS(err, 0u, code);
+}
+
+}  // namespace moe

@@ -1,0 +1,325 @@
+// Dispatch, combine and the token-major backward helpers.
+//
+// Dispatch (MoE explainer, lpnh.cn/news/725941, §3.1 Step 3 "flatten &
+// scatter") and combine (§3.1 Step 5 "gather weighted sum"; deepspeed.moe
+// overview §3.1 item 4) are HBM-bound row copies: one warp per token, rows
+// moved in 16-byte vectors, each x row read once whatever k is, each y row
+// written once (a deterministic gather, no atomics).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+// 16-byte vector of row elements and its conversion to / from fp32.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int kN = 4;
+  __device__ static void to_f32(const uint4 &u, float *o) {
+    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+    o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 from_f32(const float *v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                      __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int kN = 8;
+  __device__ static void to_f32(const uint4 &u, float *o) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static uint4 from_f32(const float *v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ int64_t row_of(const int32_t *idx, const int32_t *slot,
+                                          const int32_t *offsets, int64_t i) {
+  const int sl = slot[i];
+  return sl < 0 ? -1 : int64_t(offsets[idx[i]]) + sl;
+}
+
+// x_disp[row(s,j)] = x[s]
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+dispatch_kernel(const uint4 *__restrict__ x, int64_t S, int nvec, int k,
+                const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
+                const int32_t *__restrict__ offsets, uint4 *__restrict__ x_disp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const int64_t r0 = row_of(idx, slot, offsets, s * k);
+  const int64_t r1 = k == 2 ? row_of(idx, slot, offsets, s * k + 1) : -1;
+  if (r0 < 0 && r1 < 0) return;
+  const uint4 *src = x + s * nvec;
+  uint4 *d0 = r0 >= 0 ? x_disp + r0 * nvec : nullptr;
+  uint4 *d1 = r1 >= 0 ? x_disp + r1 * nvec : nullptr;
+  for (int c = lane; c < nvec; c += 32) {
+    const uint4 v = ld_stream(src + c);
+    if (d0) d0[c] = v;
+    if (d1) d1[c] = v;
+  }
+}
+
+// y[s] = sum_j w[s,j] * out[row(s,j)]
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
+               const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
+               const int32_t *__restrict__ offsets, const float *__restrict__ w,
+               uint4 *__restrict__ y) {
+  using V = Vec<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const int64_t r0 = row_of(idx, slot, offsets, s * k);
+  const int64_t r1 = k == 2 ? row_of(idx, slot, offsets, s * k + 1) : -1;
+  const float w0 = w[s * k];
+  const float w1 = k == 2 ? w[s * k + 1] : 0.0f;
+  for (int c = lane; c < nvec; c += 32) {
+    float acc[V::kN], t[V::kN];
+#pragma unroll
+    for (int i = 0; i < V::kN; ++i) acc[i] = 0.0f;
+    if (r0 >= 0) {
+      V::to_f32(ld_stream(out + r0 * nvec + c), t);
+#pragma unroll
+      for (int i = 0; i < V::kN; ++i) acc[i] = fmaf(w0, t[i], acc[i]);
+    }
+    if (r1 >= 0) {
+      V::to_f32(ld_stream(out + r1 * nvec + c), t);
+#pragma unroll
+      for (int i = 0; i < V::kN; ++i) acc[i] = fmaf(w1, t[i], acc[i]);
+    }
+    y[s * nvec + c] = V::from_f32(acc);
+  }
+}
+
+// dO[row] = w * dY[s]; dw[s,j] = <dY[s], out[row]>
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
+                   int64_t S, int nvec, int k, const int32_t *__restrict__ idx,
+                   const int32_t *__restrict__ slot, const int32_t *__restrict__ offsets,
+                   const float *__restrict__ w, uint4 *__restrict__ d_out,
+                   float *__restrict__ dw) {
+  using V = Vec<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  for (int j = 0; j < k; ++j) {
+    const int64_t r = row_of(idx, slot, offsets, s * k + j);
+    if (r < 0) {
+      if (lane == 0) dw[s * k + j] = 0.0f;
+      continue;
+    }
+    const float wj = w[s * k + j];
+    float dot = 0.0f;
+    for (int c = lane; c < nvec; c += 32) {
+      float g[V::kN], o[V::kN];
+      V::to_f32(dy[s * nvec + c], g);
+      V::to_f32(out[r * nvec + c], o);
+#pragma unroll
+      for (int i = 0; i < V::kN; ++i) {
+        dot = fmaf(g[i], o[i], dot);
+        g[i] *= wj;
+      }
+      d_out[r * nvec + c] = V::from_f32(g);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) dw[s * k + j] = dot;
+  }
+}
+
+// db[g, n] = sum over rows of group g of M[r, n]; blockDim (32, 8)
+__global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N,
+                                    const int32_t *__restrict__ offsets,
+                                    void *__restrict__ db) {
+  __shared__ float part[8][33];
+  const int g = blockIdx.y;
+  const int n = blockIdx.x * 32 + threadIdx.x;
+  const int64_t r0 = offsets[g], r1 = offsets[g + 1];
+  float acc = 0.0f;
+  if (n < N)
+    for (int64_t r = r0 + threadIdx.y; r < r1; r += 8) acc += load_elem(M, dtype, r * N + n);
+  part[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y == 0 && n < N) {
+    float t = 0.0f;
+    for (int i = 0; i < 8; ++i) t += part[i][threadIdx.x];
+    store_elem(db, dtype, int64_t(g) * N + n, t);
+  }
+}
+
+__global__ void first_count_kernel(const int32_t *__restrict__ idx, int64_t S, int k,
+                                   int E, int32_t *__restrict__ first) {
+  __shared__ int32_t cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int64_t s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&cnt[idx[s * k]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) first[e] = cnt[e];
+}
+
+// One warp per token; lanes over experts.
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx,
+                const float *__restrict__ dw, const int32_t *__restrict__ first,
+                int64_t S, int E, int k, float aux_scale, float *__restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const float *p = probs + s * E;
+  const int i1 = idx[s * k];
+  const int i2 = k == 2 ? idx[s * k + 1] : -1;
+  float g1, g2 = 0.0f;
+  if (k == 1) {
+    g1 = dw[s];
+  } else {
+    // w_j = p_j / (p_1 + p_2)
+    const float p1 = p[i1], p2 = p[i2];
+    const float P = p1 + p2;
+    const float inv = 1.0f / (P * P);
+    const float d = dw[s * 2] - dw[s * 2 + 1];
+    g1 = p2 * d * inv;
+    g2 = -p1 * d * inv;
+  }
+  float dot = 0.0f;
+  for (int e = lane; e < E; e += 32) {
+    float dp = aux_scale * float(first[e]);
+    if (e == i1) dp += g1;
+    if (e == i2) dp += g2;
+    dot = fmaf(dp, p[e], dot);
+  }
+  dot = warp_sum(dot);
+  for (int e = lane; e < E; e += 32) {
+    float dp = aux_scale * float(first[e]);
+    if (e == i1) dp += g1;
+    if (e == i2) dp += g2;
+    dlogits[s * E + e] = p[e] * (dp - dot);
+  }
+}
+
+// dx[s] = sum_j dx_disp[row(s,j)] + sum_e dlogits[s,e] * w_gate[e,:]
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+dx_combine_kernel(const void *__restrict__ dx_disp, const float *__restrict__ dlogits,
+                  const void *__restrict__ w_gate, int dtype, int64_t S, int d, int E,
+                  int k, const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
+                  const int32_t *__restrict__ offsets, void *__restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const int64_t r0 = row_of(idx, slot, offsets, s * k);
+  const int64_t r1 = k == 2 ? row_of(idx, slot, offsets, s * k + 1) : -1;
+  const float *dl = dlogits + s * E;
+  for (int c = lane; c < d; c += 32) {
+    float acc = 0.0f;
+    for (int e = 0; e < E; ++e) acc = fmaf(dl[e], load_elem(w_gate, dtype, int64_t(e) * d + c), acc);
+    if (r0 >= 0) acc += load_elem(dx_disp, dtype, r0 * d + c);
+    if (r1 >= 0) acc += load_elem(dx_disp, dtype, r1 * d + c);
+    store_elem(dx, dtype, s * d + c, acc);
+  }
+}
+
+inline unsigned token_blocks(int64_t S) { return unsigned((S + kWarpsPerCta - 1) / kWarpsPerCta); }
+
+}  // namespace
+
+cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
+                            const int32_t *idx, const int32_t *slot, const int32_t *offsets,
+                            void *x_disp, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const int nvec = d * elem_bytes(dtype) / 16;
+  dispatch_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+      static_cast<const uint4 *>(x), S, nvec, k, idx, slot, offsets, static_cast<uint4 *>(x_disp));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d, int k,
+                           const int32_t *idx, const int32_t *slot, const int32_t *offsets,
+                           const float *w, void *y, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const int nvec = d * elem_bytes(dtype) / 16;
+  if (dtype == MOE_F32)
+    combine_kernel<float><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+        static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
+        static_cast<uint4 *>(y));
+  else
+    combine_kernel<__nv_bfloat16><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+        static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
+        static_cast<uint4 *>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, int64_t S,
+                               int d, int k, const int32_t *idx, const int32_t *slot,
+                               const int32_t *offsets, const float *w, void *d_out, float *dw,
+                               cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const int nvec = d * elem_bytes(dtype) / 16;
+  auto *dy4 = static_cast<const uint4 *>(dy);
+  auto *o4 = static_cast<const uint4 *>(out_disp);
+  auto *do4 = static_cast<uint4 *>(d_out);
+  if (dtype == MOE_F32)
+    combine_bwd_kernel<float><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+        dy4, o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
+  else
+    combine_bwd_kernel<__nv_bfloat16><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+        dy4, o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
+                                const int32_t *offsets, void *db, cudaStream_t st) {
+  dim3 grid((N + 31) / 32, G);
+  group_colsum_kernel<<<grid, dim3(32, 8), 0, st>>>(M, dtype, N, offsets, db);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_first_count(const int32_t *idx, int64_t S, int k, int E, int32_t *first,
+                               cudaStream_t st) {
+  first_count_kernel<<<1, 1024, 0, st>>>(idx, S, k, E, first);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float *dw,
+                            const int32_t *first, int64_t S, int E, int k, float aux_w,
+                            float *dlogits, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  // d(aux_w * l_aux)/dp[s,e] = aux_w * E * first[e] / S^2
+  const float aux_scale = float(double(aux_w) * double(E) / (double(S) * double(S)));
+  gate_bwd_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(probs, idx, dw, first, S, E, k,
+                                                                 aux_scale, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits, const void *w_gate,
+                              int dtype, int64_t S, int d, int E, int k, const int32_t *idx,
+                              const int32_t *slot, const int32_t *offsets, void *dx,
+                              cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  dx_combine_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
+      dx_disp, dlogits, w_gate, dtype, S, d, E, k, idx, slot, offsets, dx);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

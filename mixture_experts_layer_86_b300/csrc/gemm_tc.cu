@@ -1,0 +1,377 @@
+// Grouped bf16 GEMM on the B300 tensor cores (tcgen05 + TMEM + TMA).
+//
+// This is the expert FFN of the MoE layer (MoE explainer, lpnh.cn/news/725941,
+// §3.1 Step 4: every expert applies Linear -> act -> Linear to the tokens it
+// received), run as ONE persistent kernel over all experts: the experts'
+// row counts live on the device (expert_offsets), so no host round trip is
+// needed between routing and the FFN.
+//
+// Tiling: 128 (rows) x 256 (n) output tile per CTA, K in 64-element (128 B)
+// slices, 4-stage TMA -> shared memory pipeline with 128-byte swizzle,
+// tcgen05.mma M=128 N=256 K=16 accumulating in TMEM, two TMEM accumulators
+// (2 x 256 columns) so the epilogue of one tile overlaps the MMAs of the
+// next.  Warp roles (192 threads):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  epilogue: tcgen05.ld -> bias / activation / dact -> bf16 ->
+//               global, rows masked to the expert's row block.
+// Tiles are ordered expert by expert, n-tile by n-tile, m fastest, so the
+// CTAs that run at the same time share weight tiles through L2.
+//
+// Every mbarrier wait is bounded: a wait that gives up records an error
+// code in the device error word, raises a CTA-wide abort flag, and the CTA
+// drains its outstanding copies / MMAs (again bounded) before freeing TMEM.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * BN;  // two accumulators
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxGroups = kMaxExperts;
+
+struct __align__(8) SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[kMaxGroups + 1];  // prefix of (m-tiles x n-tiles) over groups
+};
+
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * (kABytes + kBBytes) + sizeof(SmemCtl);
+
+struct TileCoord {
+  int g, m, n, rows;  // group, m-tile, n-tile, rows of the group
+  int row0;           // first row of the group
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const SmemCtl &c, const int32_t *offs, int G,
+                                                int nt, int t) {
+  int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  TileCoord tc;
+  tc.g = lo;
+  tc.row0 = offs[lo];
+  tc.rows = offs[lo + 1] - tc.row0;
+  const int mt = (tc.rows + BM - 1) / BM;
+  const int local = t - c.tile_start[lo];
+  tc.n = local / mt;
+  tc.m = local - tc.n * mt;
+  return tc;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &u, float *o) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool kBMN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const int32_t *__restrict__ offsets, int G, int N, int K,
+               const __nv_bfloat16 *__restrict__ bias, int act,
+               __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
+               const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * kABytes;
+  SmemCtl &ctl = *reinterpret_cast<SmemCtl *>(smem + STAGES * (kABytes + kBBytes));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (N + BN - 1) / BN;
+  const int nk = (K + BK - 1) / BK;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 128);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    int run = 0;
+    for (int g = 0; g < G; ++g) {
+      ctl.tile_start[g] = run;
+      run += ((offsets[g + 1] - offsets[g] + BM - 1) / BM) * nt;
+    }
+    ctl.tile_start[G] = run;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.tile_start[G];
+  volatile int *abort = &ctl.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // stages holding a copy not yet seen complete here
+      uint32_t armed_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(ctl, offsets, G, nt, t);
+        const int arow = tc.row0 + tc.m * BM;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kWaitLimitNs)) {
+            record_error(err, kErrGemmProducer | uint32_t(t & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, kABytes + kBBytes);
+          ptx::tma_load_2d(ptx::smem_addr(sA + stage * kABytes), &tmA, fb, kb * BK, arow);
+          if (!kBMN) {
+            ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes), &tmB, fb, kb * BK,
+                             tc.g * N + tc.n * BN);
+          } else {
+            // four 64(n) x 64(k) boxes, 8 KB apart
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes + j * (BK * 128)), &tmB, fb,
+                               tc.n * BN + j * 64, tc.g * K + kb * BK);
+          }
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let copies already issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s))
+            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+                           kWaitLimitNs / 4);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, 0, kBMN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort, kWaitLimitNs)) {
+          record_error(err, kErrGemmMma | 0x800000u | uint32_t(t & 0x7fffff));
+          *abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs)) {
+            record_error(err, kErrGemmMma | uint32_t(t & 0x7fffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_addr(sA + stage * kABytes);
+          const uint32_t b0 = ptx::smem_addr(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = kBMN ? ptx::sdesc_sw128(b0 + kk * 16 * 128, BK * 128, 1024)
+                                     : ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
+            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) ptx::mma_commit(ptx::smem_addr(&ctl.tfull[acc]));
+      }
+      // every MMA issued by this thread has finished before TMEM is freed
+      ptx::mma_commit(ptx::smem_addr(&ctl.drain));
+      if (!ptx::mbar_wait(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
+        record_error(err, kErrGemmDrain);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord(ctl, offsets, G, nt, t);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort, kWaitLimitNs)) {
+        record_error(err, kErrGemmEpilogue | uint32_t(t & 0xffffff));
+        *abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int r = tc.m * BM + r_in_tile;
+      const bool valid = r < tc.rows;
+      const int64_t grow = int64_t(tc.row0) + r;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t raw[32];
+        ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
+        ptx::tmem_ld_wait();
+        const int n0 = tc.n * BN + c * 32;
+        if (!valid || n0 >= N) continue;
+#pragma unroll
+        for (int v8 = 0; v8 < 4; ++v8) {
+          const int n = n0 + v8 * 8;
+          if (n >= N) break;
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
+          if (bias) {
+            float b[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(bias + int64_t(tc.g) * N + n), b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] += b[i];
+          }
+          const int64_t ci = grow * N + n;
+          if (pre) *reinterpret_cast<uint4 *>(pre + ci) = pack_bf16x8(x);
+          if (act >= 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = act_fwd(x[i], act);
+          }
+          if (grad_src) {
+            float z[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(grad_src + ci), z);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] *= act_grad(z[i], dact);
+          }
+          *reinterpret_cast<uint4 *>(C + ci) = pack_bf16x8(x);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&ctl.tempty[acc]));
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
+// box of [box_outer, box_inner] elements and 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
+  if (g.G <= 0 || g.G > kMaxGroups) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, BM))
+    return cudaErrorInvalidValue;
+  bool okb;
+  if (g.b_kmajor)
+    okb = make_map(&tb, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, BN);
+  else
+    okb = make_map(&tb, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
+  if (!okb) return cudaErrorInvalidValue;
+
+  static bool attr_set[2] = {false, false};
+  const int which = g.b_kmajor ? 0 : 1;
+  auto kern = g.b_kmajor ? tc_gemm_kernel<false> : tc_gemm_kernel<true>;
+  if (!attr_set[which]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set[which] = true;
+  }
+  const int grid = num_sms();
+  kern<<<grid, kThreads, kSmemBytes, st>>>(
+      ta, tb, g.offsets, g.G, g.N, g.K, static_cast<const __nv_bfloat16 *>(g.bias), g.act,
+      static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
+      static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,134 @@
+// Host-side launchers of the MoE layer kernels.  Internal header shared by
+// the kernel translation units and the C ABI (api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens per gate/routing CTA; the slot scan works on per-CTA histograms.
+constexpr int kRouteTokensPerCta = 128;
+
+// ---------------------------------------------------------------- routing
+struct RouteArgs {
+  const float *logits;  // [S,E] fp32
+  int64_t S;
+  int E, k;
+  int64_t cap;          // -1: no capacity limit
+  float *probs;         // [S,E] or null
+  int32_t *idx;         // [S,k]
+  float *w;             // [S,k]
+  int32_t *slot;        // [S,k]
+  int32_t *routed, *kept, *offsets;  // [E], [E], [E+1]
+  int32_t *row_src;     // [rows]
+  float *l_aux;
+  // workspace views
+  int32_t *hist;        // [nblk][k][E]
+  float *psum;          // [nblk][E]
+  int32_t *first_cnt;   // [E]
+};
+size_t route_workspace_bytes(int64_t S, int E, int k);
+void route_carve_workspace(RouteArgs &a, void *ws);
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+
+// ------------------------------------------------------ SIMT grouped GEMM
+// C(m,n) = epilogue( sum_k A(m,k) * B(n,k) ) with arbitrary element strides.
+//  mode 0: one GEMM of M x N x K.
+//  mode 1: row-grouped.  Rows [offsets[g], offsets[g+1]) of A and C use
+//          B + g*b_g and bias + g*bias_g.  M is unused; grid covers max_rows.
+//  mode 2: K-grouped.  C_g = sum over rows r in [offsets[g], offsets[g+1])
+//          of A(m,r) B(n,r), stored at C + g*c_g (zero when the group is
+//          empty).
+// Epilogue order: + bias (+ bias_f32), store pre (if set), act (if >= 0),
+// times act'(grad_src(m,n)) (if grad_src set, derivative of dact).
+struct SimtGemm {
+  int a_dtype, b_dtype, c_dtype;
+  const void *A; int64_t a_m, a_k;
+  const void *B; int64_t b_n, b_k, b_g;
+  void *C; int64_t c_m, c_n, c_g;
+  int64_t M; int N, K;
+  int mode;
+  const int32_t *offsets; int G;
+  int64_t max_rows;
+  const void *bias; int64_t bias_g;     // element type b_dtype
+  const float *bias_f32;                // fp32 bias over n (mode 0)
+  int act;                              // -1 none
+  void *pre;                            // same layout/type as C
+  const void *grad_src; int dact;       // same layout/type as C
+};
+cudaError_t launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
+
+// ------------------------------------------------ tcgen05 grouped GEMM
+// Row-grouped bf16 GEMM on the 5th-generation tensor cores:
+//   C[r, n] = epi( sum_k A[r, k] * B_g(n, k) )  for r in group g's rows,
+// A: [rows, K] bf16 row-major.  B_g: rows g*N .. g*N+N-1 of a [G*N, K]
+// (b_kmajor) or columns of a [G*K, N] (!b_kmajor) bf16 matrix.
+// Epilogue: + bias[g*N + n] (bf16, nullable), store pre (bf16, nullable),
+// act (>= 0), times act'(grad_src[r, n]) when grad_src is set; C bf16.
+struct TcGemm {
+  const void *A; int64_t rows_alloc;   // rows of the A/C allocations
+  const void *B; bool b_kmajor;
+  void *C;
+  int N, K, G;
+  const int32_t *offsets;
+  const void *bias;
+  int act;
+  void *pre;
+  const void *grad_src; int dact;
+  unsigned int *err;
+};
+cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
+
+// K-grouped bf16 weight-gradient GEMM on the tensor cores:
+//   C_g[m, n] = sum over rows r of group g of A[r, m] * B[r, n]
+// A: [rows, M] bf16, B: [rows, N] bf16 (both row-major), C: [G, M, N] bf16.
+struct TcWgrad {
+  const void *A; const void *B; int64_t rows_alloc;
+  void *C;
+  int M, N, G;
+  const int32_t *offsets;
+  unsigned int *err;
+};
+cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);
+
+// ------------------------------------------------ dispatch / combine
+cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
+                            const int32_t *idx, const int32_t *slot,
+                            const int32_t *offsets, void *x_disp, cudaStream_t st);
+cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d,
+                           int k, const int32_t *idx, const int32_t *slot,
+                           const int32_t *offsets, const float *w, void *y,
+                           cudaStream_t st);
+
+// ------------------------------------------------ backward helpers
+// dO[row] = w * dY[s], dw[s,j] = <dY[s], out[row]> (0 when dropped).
+cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype,
+                               int64_t S, int d, int k, const int32_t *idx,
+                               const int32_t *slot, const int32_t *offsets,
+                               const float *w, void *d_out, float *dw,
+                               cudaStream_t st);
+// db[g, n] = sum over group rows of M[r, n]  (zero for empty groups).
+cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
+                                const int32_t *offsets, void *db,
+                                cudaStream_t st);
+// first[e] = number of tokens whose first choice is e.
+cudaError_t launch_first_count(const int32_t *idx, int64_t S, int k, int E,
+                               int32_t *first, cudaStream_t st);
+// dlogits = p * (dp - <dp,p>), dp from dw through the weights and the
+// l_aux term aux_w * E * first[e] / S^2.
+cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx,
+                            const float *dw, const int32_t *first, int64_t S,
+                            int E, int k, float aux_w, float *dlogits,
+                            cudaStream_t st);
+// dx[s] = sum_j dx_disp[row(s,j)] + dlogits[s] . w_gate
+cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits,
+                              const void *w_gate, int dtype, int64_t S, int d,
+                              int E, int k, const int32_t *idx,
+                              const int32_t *slot, const int32_t *offsets,
+                              void *dx, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

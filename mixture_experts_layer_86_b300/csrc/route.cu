@@ -1,0 +1,280 @@
+// Routing: softmax, top-k, combine weights, capacity-limited slot
+// assignment in priority order, counts, offsets and l_aux.
+//
+// MoE explainer (lpnh.cn/news/725941) §3.1 Step 2 (top-k, softmax over the
+// selected logits), DeepSeek-MoE page (lnwmold.com/news/1162317) ch.1
+// (softmax -> top-2, capacity = ceil(S*2/E*cf)), deepspeed.moe overview
+// (adg.csdn.net/694deb285b9f5f31781ae763) §2.1 (min_capacity, drop_tokens,
+// gate_loss, expert_count).
+//
+// Three kernels, no atomics (the result is the same on every run):
+//  1. route_topk: one CTA per 128 tokens.  Per token (one warp): softmax,
+//     top-k with ties to the lower expert index, weights.  Per CTA: the
+//     count of each (choice j, expert e) pair, the rank of each token among
+//     the CTA's tokens with the same (j, e) (kept in `slot` for now), and
+//     the CTA's sum of probabilities per expert.
+//  2. route_scan: one CTA.  Exclusive scan of the per-CTA counts over CTAs
+//     for every (j, e); totals; routed / kept counts; offsets; l_aux.
+//  3. route_assign: slot = (first-choice total of e if j == 1) + scanned
+//     base + CTA rank.  Every first choice therefore precedes every second
+//     choice, each in token order.  slot >= C -> -1; row_src of kept rows.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTB = kRouteTokensPerCta;  // tokens per CTA
+constexpr int kWarps = kTB / 32;         // warps per CTA (one lane per token in phase 2)
+constexpr int kMaxPerLane = kMaxExperts / 32;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__global__ void __launch_bounds__(kTB)
+route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
+                  float *__restrict__ probs, int32_t *__restrict__ idx_out,
+                  float *__restrict__ w_out, int32_t *__restrict__ rank_out,
+                  int32_t *__restrict__ hist, float *__restrict__ psum) {
+  __shared__ int32_t s_choice[2][kTB];
+  __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
+  __shared__ float s_psum[kWarps][kMaxExperts];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tok0 = int64_t(blockIdx.x) * kTB;
+  const int nq = (E + 31) >> 5;
+
+  float pacc[kMaxPerLane];
+#pragma unroll
+  for (int q = 0; q < kMaxPerLane; ++q) pacc[q] = 0.0f;
+
+  // ---- phase 1: one warp per token, lanes over experts
+  for (int t = warp; t < kTB; t += kWarps) {
+    const int64_t s = tok0 + t;
+    if (s >= S) {
+      if (lane == 0) {
+        s_choice[0][t] = -1;
+        s_choice[1][t] = -1;
+      }
+      continue;
+    }
+    const float *row = logits + s * E;
+    float v[kMaxPerLane];
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const int e = lane + 32 * q;
+      v[q] = (q < nq && e < E) ? row[e] : -INFINITY;
+      m = fmaxf(m, v[q]);
+    }
+    m = warp_max(m);
+    float ex[kMaxPerLane];
+    float z = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const int e = lane + 32 * q;
+      ex[q] = (q < nq && e < E) ? expf(v[q] - m) : 0.0f;
+      z += ex[q];
+    }
+    z = warp_sum(z);
+    const float inv_z = 1.0f / z;
+    // top-1 (ties -> lower index)
+    float b1 = -INFINITY;
+    int i1 = -1;
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const int e = lane + 32 * q;
+      if (q < nq && e < E && (i1 < 0 || v[q] > b1)) {
+        b1 = v[q];
+        i1 = e;
+      }
+    }
+    warp_argmax(b1, i1);
+    int i2 = -1;
+    if (k == 2) {
+      float b2 = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kMaxPerLane; ++q) {
+        const int e = lane + 32 * q;
+        if (q < nq && e < E && e != i1 && (i2 < 0 || v[q] > b2)) {
+          b2 = v[q];
+          i2 = e;
+        }
+      }
+      warp_argmax(b2, i2);
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const int e = lane + 32 * q;
+      if (q < nq && e < E) {
+        const float p = ex[q] * inv_z;
+        pacc[q] += p;
+        if (probs) probs[s * E + e] = p;
+      }
+    }
+    // exp(l - max) of the chosen experts, broadcast from the lanes holding them
+    float x1 = 0.0f, x2 = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const float a = __shfl_sync(kFullMask, ex[q], i1 & 31);
+      if ((i1 >> 5) == q) x1 = a;
+      if (k == 2) {
+        const float b = __shfl_sync(kFullMask, ex[q], i2 & 31);
+        if ((i2 >> 5) == q) x2 = b;
+      }
+    }
+    if (lane == 0) {
+      s_choice[0][t] = i1;
+      idx_out[s * k] = i1;
+      if (k == 1) {
+        w_out[s] = x1 * inv_z;
+        s_choice[1][t] = -1;
+      } else {
+        const float den = x1 + x2;
+        w_out[s * 2] = x1 / den;
+        w_out[s * 2 + 1] = x2 / den;
+        idx_out[s * 2 + 1] = i2;
+        s_choice[1][t] = i2;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxPerLane; ++q) {
+    const int e = lane + 32 * q;
+    if (q < nq && e < E) s_psum[warp][e] = pacc[q];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTB) {
+    float acc = 0.0f;
+    for (int w = 0; w < kWarps; ++w) acc += s_psum[w][e];
+    psum[int64_t(blockIdx.x) * E + e] = acc;
+  }
+
+  // ---- phase 2: one lane per token; rank among equal (j, e) in token order
+  const int t = threadIdx.x;
+  const int64_t s = tok0 + t;
+  for (int j = 0; j < k; ++j) {
+    for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += kTB) (&s_wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const int e = s_choice[j][t];
+    const unsigned peers = __match_any_sync(kFullMask, e);
+    const int rank = __popc(peers & lanemask_lt());
+    if (e >= 0 && rank == 0) s_wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    for (int ee = threadIdx.x; ee < E; ee += kTB) {
+      int run = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        const int c = s_wcnt[w][ee];
+        s_wcnt[w][ee] = run;
+        run += c;
+      }
+      hist[(int64_t(blockIdx.x) * k + j) * E + ee] = run;
+    }
+    __syncthreads();
+    if (e >= 0 && s < S) rank_out[s * k + j] = s_wcnt[warp][e] + rank;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(512)
+route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
+                  int32_t *__restrict__ hist, const float *__restrict__ psum,
+                  int32_t *__restrict__ first_cnt, int32_t *__restrict__ routed,
+                  int32_t *__restrict__ kept, int32_t *__restrict__ offsets,
+                  float *__restrict__ l_aux) {
+  __shared__ int32_t s_tot[2][kMaxExperts];
+  __shared__ double s_aux[kMaxExperts];
+  const int t = threadIdx.x;
+  if (t < k * E) {
+    const int j = t / E, e = t % E;
+    int run = 0;
+    for (int64_t b = 0; b < nblk; ++b) {
+      int32_t *p = hist + (b * k + j) * E + e;
+      const int c = *p;
+      *p = run;
+      run += c;
+    }
+    s_tot[j][e] = run;
+  }
+  __syncthreads();
+  if (t < E) {
+    const int r = s_tot[0][t] + (k == 2 ? s_tot[1][t] : 0);
+    routed[t] = r;
+    kept[t] = (cap < 0 || r < cap) ? r : int(cap);
+    first_cnt[t] = s_tot[0][t];
+    double ps = 0.0;
+    for (int64_t b = 0; b < nblk; ++b) ps += double(psum[b * E + t]);
+    s_aux[t] = ps * double(s_tot[0][t]);
+  }
+  __syncthreads();
+  if (t == 0) {
+    int run = 0;
+    double aux = 0.0;
+    for (int e = 0; e < E; ++e) {
+      offsets[e] = run;
+      const int r = s_tot[0][e] + (k == 2 ? s_tot[1][e] : 0);
+      run += (cap < 0 || r < cap) ? r : int(cap);
+      aux += s_aux[e];
+    }
+    offsets[E] = run;
+    // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
+    *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
+  }
+}
+
+__global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap,
+                                    const int32_t *__restrict__ idx,
+                                    const int32_t *__restrict__ hist,
+                                    const int32_t *__restrict__ first_cnt,
+                                    const int32_t *__restrict__ offsets,
+                                    int32_t *__restrict__ slot,
+                                    int32_t *__restrict__ row_src) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= S * k) return;
+  const int64_t s = i / k;
+  const int j = int(i - s * k);
+  const int e = idx[i];
+  const int64_t b = s / kTB;
+  const int pos = hist[(b * k + j) * E + e] + (j == 1 ? first_cnt[e] : 0) + slot[i];
+  if (cap < 0 || pos < cap) {
+    slot[i] = pos;
+    row_src[offsets[e] + pos] = int32_t(i);
+  } else {
+    slot[i] = -1;
+  }
+}
+
+}  // namespace
+
+size_t route_workspace_bytes(int64_t S, int E, int k) {
+  const int64_t nblk = (S + kTB - 1) / kTB;
+  return align256(size_t(nblk) * k * E * 4) + align256(size_t(nblk) * E * 4) +
+         align256(size_t(E) * 4);
+}
+
+void route_carve_workspace(RouteArgs &a, void *ws) {
+  const int64_t nblk = (a.S + kTB - 1) / kTB;
+  char *p = static_cast<char *>(ws);
+  a.hist = reinterpret_cast<int32_t *>(p);
+  p += align256(size_t(nblk) * a.k * a.E * 4);
+  a.psum = reinterpret_cast<float *>(p);
+  p += align256(size_t(nblk) * a.E * 4);
+  a.first_cnt = reinterpret_cast<int32_t *>(p);
+}
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
+  const int64_t nblk = (a.S + kTB - 1) / kTB;
+  if (nblk > 0) {
+    route_topk_kernel<<<unsigned(nblk), kTB, 0, st>>>(a.logits, a.S, a.E, a.k, a.probs,
+                                                     a.idx, a.w, a.slot, a.hist, a.psum);
+  }
+  route_scan_kernel<<<1, 512, 0, st>>>(nblk, a.S, a.E, a.k, a.cap, a.hist, a.psum,
+                                       a.first_cnt, a.routed, a.kept, a.offsets, a.l_aux);
+  const int64_t n = a.S * a.k;
+  if (n > 0) {
+    route_assign_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
+        a.S, a.E, a.k, a.cap, a.idx, a.hist, a.first_cnt, a.offsets, a.slot, a.row_src);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

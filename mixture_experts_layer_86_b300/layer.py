@@ -1,0 +1,73 @@
+"""Allocation helpers around the C ABI: the caller-side memory plan of one
+MoE layer call (torch allocates, the library computes).
+
+``forward`` returns ``(y, l_aux, expert_count, state)`` like MoE.forward's
+``(output, gate_loss, expert_count)`` on the deepspeed.moe overview page
+(§2.1); ``backward`` returns the gradients of <dY, y> + aux_loss_weight*l_aux.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native as N
+
+
+def torch_dtype(cfg: N.MoeConfig) -> torch.dtype:
+    return torch.float32 if cfg.dtype == N.MOE_F32 else torch.bfloat16
+
+
+def alloc_buffers(cfg: N.MoeConfig, device, training: bool = False) -> dict:
+    """Device buffers of one forward pass, sized from the config alone."""
+    S, E, k = cfg.num_tokens, cfg.num_experts, cfg.k
+    d, f = cfg.hidden_size, cfg.ffn_size
+    R = N.moe_max_rows(cfg)
+    dt = torch_dtype(cfg)
+    i32 = dict(dtype=torch.int32, device=device)
+    f32 = dict(dtype=torch.float32, device=device)
+    return {
+        "logits": torch.empty((S, E), **f32),
+        "probs": torch.empty((S, E), **f32) if training else None,
+        "topk_idx": torch.empty((S, k), **i32),
+        "topk_w": torch.empty((S, k), **f32),
+        "slot": torch.empty((S, k), **i32),
+        "routed_cnt": torch.empty((E,), **i32),
+        "kept_cnt": torch.empty((E,), **i32),
+        "expert_offsets": torch.empty((E + 1,), **i32),
+        "row_src": torch.empty((max(R, 1),), **i32),
+        "l_aux": torch.empty((1,), **f32),
+        "x_disp": torch.empty((max(R, 1), d), dtype=dt, device=device),
+        "h_pre": torch.empty((max(R, 1), f), dtype=dt, device=device) if training else None,
+        "h": torch.empty((max(R, 1), f), dtype=dt, device=device),
+        "out_disp": torch.empty((max(R, 1), d), dtype=dt, device=device),
+    }
+
+
+def alloc_workspace(cfg: N.MoeConfig, device, for_backward: bool = False) -> torch.Tensor:
+    n = N.moe_workspace_size(cfg, for_backward)
+    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device)
+
+
+def forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, bufs=None, workspace=None,
+            y=None, training=False, stream=None):
+    dev = x.device
+    if bufs is None:
+        bufs = alloc_buffers(cfg, dev, training)
+    if workspace is None:
+        workspace = alloc_workspace(cfg, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    N.moe_forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, y, bufs, workspace, stream)
+    return y, bufs["l_aux"], bufs["kept_cnt"], bufs
+
+
+def backward(cfg, x, w_gate, w1, w2, bufs, dy, workspace=None, grads=None, stream=None):
+    dev = x.device
+    if workspace is None:
+        workspace = alloc_workspace(cfg, dev, for_backward=True)
+    if grads is None:
+        grads = {"dx": torch.empty_like(x), "dw_gate": torch.empty_like(w_gate),
+                 "dw1": torch.empty_like(w1), "db1": torch.empty(w1.shape[:2], dtype=w1.dtype, device=dev),
+                 "dw2": torch.empty_like(w2), "db2": torch.empty(w2.shape[:2], dtype=w2.dtype, device=dev)}
+    N.moe_backward(cfg, x, w_gate, w1, w2, bufs, dy, grads["dx"], grads["dw_gate"], grads["dw1"],
+                   grads["db1"], grads["dw2"], grads["db2"], workspace, stream)
+    return grads
