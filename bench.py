@@ -1,0 +1,408 @@
+"""Throughput of the MoE layer forward on B300, one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one forward pass of the whole layer (gate GEMM, softmax / top-k /
+capacity / slots, dispatch, grouped expert FFN, combine) over one batch of
+synthetic input, through the library's C ABI.  The default workload is the
+64-expert layer (S=16384, d=2048, E=64, f=5120, top-2, cf=1.25, bf16).
+
+Multi-GPU: the layer does not shard in this library, so N GPUs run N
+independent replicas (one process per GPU under torchrun); `value` is the
+tokens all ranks processed over the max-over-ranks time.
+
+`--impl reference` times the float64 CPU oracle instead (rank 0 only), on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (bf16 fwd/fwd+bwd); % of BF16 TC peak and HBM GB/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+GEMM_SOURCES = ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "kernels.h"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def gemm_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "mixture_experts_layer_86_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, rows: int):
+    """DRAM bytes per GEMM launch from the committed ncu summary, scaled to
+    this launch's rows; None if the kernel source changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as fh:
+        d = json.load(fh)
+    ent = d.get("tc_gemm_kernel")
+    if not ent or ent.get("source_sha") != gemm_source_sha() or ent.get("workload") != workload:
+        return None
+    return int(ent["dram_bytes_per_launch"])
+
+
+def workload_desc(wl) -> str:
+    return (f"{wl.name}: MoE layer forward S={wl.num_tokens} d={wl.hidden_size} "
+            f"E={wl.num_experts} f={wl.ffn_size} top-{wl.k} cf={wl.capacity_factor} "
+            f"min_cap={wl.min_capacity} drop={wl.drop_tokens} {wl.act} {wl.dtype}")
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_layer_86_b300 import _native as N
+    from mixture_experts_layer_86_b300 import layer as L
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    wl = WORKLOADS[args.workload]
+    cfg = N.config_from_workload(wl)
+    inp_cpu = make_inputs(wl)
+    d = inp_cpu.to(dev)
+    bufs = L.alloc_buffers(cfg, dev)
+    ws = L.alloc_workspace(cfg, dev)
+    y = torch.empty_like(d.x)
+    st = torch.cuda.current_stream()
+    S, dm, f, E, k = wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k
+    eb = 2 if wl.dtype == "bf16" else 4
+
+    def step():
+        N.moe_forward(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, y, bufs, ws, st)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    R = int(bufs["expert_offsets"][-1].item())
+
+    # ---- value: K steps through moe_forward, inputs resident in HBM
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+
+    # ---- per-stage times: the same kernels through the stage entry points
+    n_ev = 5
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        ev = evs[i]
+        ev[0].record(st)
+        N.moe_gate_topk(cfg, d.x, d.w_gate, d.logit_bias, bufs["logits"], None, bufs["topk_idx"],
+                        bufs["topk_w"], bufs["slot"], bufs["routed_cnt"], bufs["kept_cnt"],
+                        bufs["expert_offsets"], bufs["row_src"], bufs["l_aux"], ws, st)
+        ev[1].record(st)
+        N.moe_dispatch(cfg, d.x, bufs["topk_idx"], bufs["slot"], bufs["expert_offsets"],
+                       bufs["x_disp"], st)
+        ev[2].record(st)
+        N.moe_expert_ffn(cfg, bufs["x_disp"], bufs["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
+                         None, bufs["h"], bufs["out_disp"], st)
+        ev[3].record(st)
+        N.moe_combine(cfg, bufs["out_disp"], bufs["topk_idx"], bufs["slot"],
+                      bufs["expert_offsets"], bufs["topk_w"], y, st)
+        ev[4].record(st)
+    torch.cuda.synchronize()
+    stage_ms = {name: statistics.median(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
+                for j, name in enumerate(["gate", "dispatch", "expert_ffn", "combine"])}
+
+    # ---- e2e: host buffers, copies inside the timed region
+    x_host = inp_cpu.x.pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    laux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
+    kept_host = torch.empty((E,), dtype=torch.int32).pin_memory()
+    x_dev = torch.empty_like(d.x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        N.moe_forward(cfg, x_dev, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, y, bufs, ws, st)
+        y_host.copy_(y, non_blocking=True)
+        laux_host.copy_(bufs["l_aux"], non_blocking=True)
+        kept_host.copy_(bufs["kept_cnt"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    flops_launch = 2.0 * R * dm * f           # one of the two equal expert GEMMs
+    gemm_launch_ms = stage_ms["expert_ffn"] / 2.0
+    achieved = flops_launch / (gemm_launch_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(wl.name, R)
+    hbm_peak = peaks["hbm_gbs"]
+
+    def gbs(nbytes, ms_):
+        return nbytes / (ms_ * 1e-3) / 1e9
+
+    gate_bytes = S * dm * eb + E * dm * eb + S * E * 4 + S * k * 12
+    disp_bytes = S * dm * eb + R * dm * eb + S * k * 8
+    comb_bytes = R * dm * eb + S * dm * eb + S * k * 12
+    stages = {
+        "gate": {"ms": stage_ms["gate"], "GB/s": gbs(gate_bytes, stage_ms["gate"]),
+                 "frac_hbm": gbs(gate_bytes, stage_ms["gate"]) / hbm_peak},
+        "dispatch": {"ms": stage_ms["dispatch"], "GB/s": gbs(disp_bytes, stage_ms["dispatch"]),
+                     "frac_hbm": gbs(disp_bytes, stage_ms["dispatch"]) / hbm_peak},
+        "expert_ffn": {"ms": stage_ms["expert_ffn"],
+                       "TFLOP/s": 2 * flops_launch / (stage_ms["expert_ffn"] * 1e-3) / 1e12},
+        "combine": {"ms": stage_ms["combine"], "GB/s": gbs(comb_bytes, stage_ms["combine"]),
+                    "frac_hbm": gbs(comb_bytes, stage_ms["combine"]) / hbm_peak},
+    }
+    launches_per_step = 8  # gate GEMM, route x3, dispatch, 2 expert GEMMs, combine
+    line = {
+        "metric": METRIC,
+        "value": world * S * args.steps / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": workload_desc(wl), "rows_kept": R,
+                   "capacity": N.moe_capacity(cfg),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: each step streams 2.7 GB of expert weights, 21x the 126 MB L2"},
+        "roofline": {"bound": "tensor", "kernel": "tc_gemm_kernel (expert GEMM, one launch)",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "frac_sustained": achieved / peaks.get("bf16_tflops_sustained",
+                                                            peaks["bf16_tflops"]),
+                     "peak_source": f"{peak_src} (dense bf16 burst)",
+                     "flops_per_launch": flops_launch,
+                     "launch_ms": gemm_launch_ms,
+                     "traffic": traffic},
+        "stages": stages,
+        "e2e": {"value": world * S * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": S * dm * eb,
+                "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu_baseline(wl, inp_cpu, args),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------- CPU oracle
+def _oracle_forward_tokens(wl, inp_cpu, n):
+    import torch
+    from oracle import moe_oracle as O
+    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    cfg = O.LayerConfig(n, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k,
+                        wl.capacity_factor, wl.min_capacity, wl.drop_tokens, wl.act)
+    lb = None if inp_cpu.logit_bias is None else f64(inp_cpu.logit_bias)
+    return O.forward(cfg, f64(inp_cpu.x[:n]), f64(inp_cpu.w_gate), inp_cpu.w1_f64,
+                     inp_cpu.b1_f64, inp_cpu.w2_f64, inp_cpu.b2_f64, logit_bias=lb)
+
+
+def _prepare_oracle_weights(inp_cpu):
+    # exact float32 copies of the bf16 weights; the oracle widens each
+    # expert's slice to float64 itself
+    import torch
+    if not hasattr(inp_cpu, "w1_f64"):
+        inp_cpu.w1_f64 = inp_cpu.w1.to(torch.float32).numpy()
+        inp_cpu.b1_f64 = inp_cpu.b1.to(torch.float32).numpy()
+        inp_cpu.w2_f64 = inp_cpu.w2.to(torch.float32).numpy()
+        inp_cpu.b2_f64 = inp_cpu.b2.to(torch.float32).numpy()
+
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else (os.cpu_count() or 1)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, inp_cpu, args, budget_s: float = 15.0):
+    """The oracle, as it stands, on the first n tokens of the same workload,
+    n chosen from a short probe so the timed run takes about budget_s."""
+    _prepare_oracle_weights(inp_cpu)
+    t0 = time.perf_counter()
+    _oracle_forward_tokens(wl, inp_cpu, 64)
+    per_tok = (time.perf_counter() - t0) / 64
+    n = int(min(wl.num_tokens, max(64, budget_s / max(per_tok, 1e-9))))
+    t0 = time.perf_counter()
+    _oracle_forward_tokens(wl, inp_cpu, n)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"float64 oracle forward on the first {n} of {wl.num_tokens} tokens "
+                      f"(same layer, capacity recomputed for the sample), {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+    wl = WORKLOADS[args.workload]
+    inp_cpu = make_inputs(wl)
+    _prepare_oracle_weights(inp_cpu)
+    t0 = time.perf_counter()
+    _oracle_forward_tokens(wl, inp_cpu, 32)
+    per_tok = (time.perf_counter() - t0) / 32
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    n = int(min(wl.num_tokens, max(8, per_step / max(per_tok, 1e-9))))
+    for _ in range(args.warmup):
+        _oracle_forward_tokens(wl, inp_cpu, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_forward_tokens(wl, inp_cpu, n)
+    dt = time.perf_counter() - t0
+    v = n * args.steps / dt
+    sample = (f"float64 oracle forward on the first {n} of {wl.num_tokens} tokens per step "
+              f"(same layer, capacity recomputed for the sample)")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "tokens_per_step": n},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _blas_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="e64_bf16")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -254,6 +254,21 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x, const void *w_gat
       !ok_ptr(l_aux) || !ok_ptr(workspace))
     return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < fwd_ws_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  if (cfg->dtype == MOE_BF16) {
+    // fused tensor-core gate, then the shared scan / assignment
+    RouteArgs a{};
+    a.S = cfg->num_tokens; a.E = cfg->num_experts; a.k = cfg->k; a.cap = capacity_of(cfg);
+    a.probs = probs; a.idx = topk_idx; a.w = topk_w; a.slot = slot; a.routed = routed_cnt;
+    a.kept = kept_cnt; a.offsets = expert_offsets; a.row_src = row_src; a.l_aux = l_aux;
+    route_carve_workspace(a, workspace);
+    GateTcArgs g{};
+    g.x = x; g.w_gate = w_gate; g.S = cfg->num_tokens; g.d = cfg->hidden_size;
+    g.E = cfg->num_experts; g.k = cfg->k; g.logit_bias = logit_bias; g.logits = logits;
+    g.probs = probs; g.idx = topk_idx; g.w = topk_w; g.rank = slot; g.hist = a.hist;
+    g.psum = a.psum; g.err = device_error_ptr();
+    MOE_CUDA(launch_gate_tc(g, stream));
+    return cuda_status(launch_route_finish(a, stream));
+  }
   float *lg = logits;
   if (!lg)
     lg = reinterpret_cast<float *>(static_cast<char *>(workspace) +

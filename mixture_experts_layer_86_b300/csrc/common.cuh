@@ -95,6 +95,9 @@ enum : uint32_t {
   kErrGemmMma = 0x02000000u,
   kErrGemmEpilogue = 0x03000000u,
   kErrGemmDrain = 0x04000000u,
+  kErrGateProducer = 0x05000000u,
+  kErrGateMma = 0x06000000u,
+  kErrGateEpilogue = 0x07000000u,
 };
 
 __device__ __forceinline__ void record_error(unsigned int *err, uint32_t code) {

@@ -25,13 +25,32 @@ struct RouteArgs {
   int32_t *row_src;     // [rows]
   float *l_aux;
   // workspace views
-  int32_t *hist;        // [nblk][k][E]
-  float *psum;          // [nblk][E]
+  int32_t *hist;        // [k][E][nblk] per-CTA counts, then their scan
+  float *psum;          // [E][nblk] per-CTA probability sums
   int32_t *first_cnt;   // [E]
 };
 size_t route_workspace_bytes(int64_t S, int E, int k);
 void route_carve_workspace(RouteArgs &a, void *ws);
+// steps 1-3 from fp32 logits in memory
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+// steps 2-3 only (after the fused gate wrote the per-CTA counts)
+cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st);
+
+// Fused bf16 gate: router GEMM on the tensor cores + routing step 1.
+struct GateTcArgs {
+  const void *x, *w_gate;   // bf16 [S,d], [E,d]
+  int64_t S;
+  int d, E, k;
+  const float *logit_bias;  // [E] or null
+  float *logits, *probs;    // [S,E] or null
+  int32_t *idx;
+  float *w;
+  int32_t *rank;            // the slot buffer, holding CTA ranks until step 3
+  int32_t *hist;
+  float *psum;
+  unsigned int *err;
+};
+cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st);
 
 // ------------------------------------------------------ SIMT grouped GEMM
 // C(m,n) = epilogue( sum_k A(m,k) * B(n,k) ) with arbitrary element strides.

@@ -7,14 +7,16 @@
 // (adg.csdn.net/694deb285b9f5f31781ae763) §2.1 (min_capacity, drop_tokens,
 // gate_loss, expert_count).
 //
-// Three kernels, no atomics (the result is the same on every run):
-//  1. route_topk: one CTA per 128 tokens.  Per token (one warp): softmax,
-//     top-k with ties to the lower expert index, weights.  Per CTA: the
-//     count of each (choice j, expert e) pair, the rank of each token among
-//     the CTA's tokens with the same (j, e) (kept in `slot` for now), and
-//     the CTA's sum of probabilities per expert.
-//  2. route_scan: one CTA.  Exclusive scan of the per-CTA counts over CTAs
-//     for every (j, e); totals; routed / kept counts; offsets; l_aux.
+// Three steps, no atomics (the result is the same on every run):
+//  1. per CTA of 128 tokens: softmax, top-k with ties to the lower expert
+//     index, weights; the count of each (choice j, expert e) pair in the
+//     CTA, the rank of each token among the CTA's tokens with the same
+//     (j, e) (kept in `slot` for now), and the CTA's per-expert sum of
+//     probabilities.  Done by route_topk (fp32 logits in memory) or by the
+//     fused tensor-core gate (gate_tc.cu).  Counts are stored column-major,
+//     hist[(j*E + e)*nblk + cta], so each (j, e) column is contiguous.
+//  2. route_scan (one CTA): exclusive scan of every column over CTAs, in
+//     place; totals; routed / kept counts; offsets; l_aux.
 //  3. route_assign: slot = (first-choice total of e if j == 1) + scanned
 //     base + CTA rank.  Every first choice therefore precedes every second
 //     choice, each in token order.  slot >= C -> -1; row_src of kept rows.
@@ -146,7 +148,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
   for (int e = threadIdx.x; e < E; e += kTB) {
     float acc = 0.0f;
     for (int w = 0; w < kWarps; ++w) acc += s_psum[w][e];
-    psum[int64_t(blockIdx.x) * E + e] = acc;
+    psum[int64_t(e) * gridDim.x + blockIdx.x] = acc;
   }
 
   // ---- phase 2: one lane per token; rank among equal (j, e) in token order
@@ -167,7 +169,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
         s_wcnt[w][ee] = run;
         run += c;
       }
-      hist[(int64_t(blockIdx.x) * k + j) * E + ee] = run;
+      hist[(int64_t(j) * E + ee) * gridDim.x + blockIdx.x] = run;
     }
     __syncthreads();
     if (e >= 0 && s < S) rank_out[s * k + j] = s_wcnt[warp][e] + rank;
@@ -175,7 +177,31 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
   }
 }
 
-__global__ void __launch_bounds__(512)
+constexpr int kScanThreads = 1024;
+
+// Exclusive scan of one contiguous column of n counts by one warp: lane l
+// owns blocks [l*per, (l+1)*per).  Returns the column total.
+__device__ int warp_scan_column(int32_t *col, int64_t n, int lane) {
+  const int64_t per = (n + 31) / 32;
+  const int64_t b0 = lane * per, b1 = min(n, b0 + per);
+  int local = 0;
+  for (int64_t b = b0; b < b1; ++b) local += col[b];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int run = incl - local;
+  for (int64_t b = b0; b < b1; ++b) {
+    const int c = col[b];
+    col[b] = run;
+    run += c;
+  }
+  return __shfl_sync(kFullMask, incl, 31);
+}
+
+__global__ void __launch_bounds__(kScanThreads)
 route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
                   int32_t *__restrict__ hist, const float *__restrict__ psum,
                   int32_t *__restrict__ first_cnt, int32_t *__restrict__ routed,
@@ -183,29 +209,27 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
                   float *__restrict__ l_aux) {
   __shared__ int32_t s_tot[2][kMaxExperts];
   __shared__ double s_aux[kMaxExperts];
-  const int t = threadIdx.x;
-  if (t < k * E) {
-    const int j = t / E, e = t % E;
-    int run = 0;
-    for (int64_t b = 0; b < nblk; ++b) {
-      int32_t *p = hist + (b * k + j) * E + e;
-      const int c = *p;
-      *p = run;
-      run += c;
-    }
-    s_tot[j][e] = run;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kW = kScanThreads / 32;
+  for (int col = warp; col < k * E; col += kW) {
+    const int tot = warp_scan_column(hist + int64_t(col) * nblk, nblk, lane);
+    if (lane == 0) s_tot[col / E][col % E] = tot;
+  }
+  for (int e = warp; e < E; e += kW) {
+    double ps = 0.0;
+    for (int64_t b = lane; b < nblk; b += 32) ps += double(psum[int64_t(e) * nblk + b]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(kFullMask, ps, o);
+    if (lane == 0) s_aux[e] = ps;
   }
   __syncthreads();
+  const int t = threadIdx.x;
   if (t < E) {
     const int r = s_tot[0][t] + (k == 2 ? s_tot[1][t] : 0);
     routed[t] = r;
     kept[t] = (cap < 0 || r < cap) ? r : int(cap);
     first_cnt[t] = s_tot[0][t];
-    double ps = 0.0;
-    for (int64_t b = 0; b < nblk; ++b) ps += double(psum[b * E + t]);
-    s_aux[t] = ps * double(s_tot[0][t]);
   }
-  __syncthreads();
   if (t == 0) {
     int run = 0;
     double aux = 0.0;
@@ -213,7 +237,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
       offsets[e] = run;
       const int r = s_tot[0][e] + (k == 2 ? s_tot[1][e] : 0);
       run += (cap < 0 || r < cap) ? r : int(cap);
-      aux += s_aux[e];
+      aux += s_aux[e] * double(s_tot[0][e]);
     }
     offsets[E] = run;
     // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
@@ -221,7 +245,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
   }
 }
 
-__global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap,
+__global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap, int64_t nblk,
                                     const int32_t *__restrict__ idx,
                                     const int32_t *__restrict__ hist,
                                     const int32_t *__restrict__ first_cnt,
@@ -234,7 +258,7 @@ __global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap,
   const int j = int(i - s * k);
   const int e = idx[i];
   const int64_t b = s / kTB;
-  const int pos = hist[(b * k + j) * E + e] + (j == 1 ? first_cnt[e] : 0) + slot[i];
+  const int pos = hist[(int64_t(j) * E + e) * nblk + b] + (j == 1 ? first_cnt[e] : 0) + slot[i];
   if (cap < 0 || pos < cap) {
     slot[i] = pos;
     row_src[offsets[e] + pos] = int32_t(i);
@@ -261,20 +285,27 @@ void route_carve_workspace(RouteArgs &a, void *ws) {
   a.first_cnt = reinterpret_cast<int32_t *>(p);
 }
 
+cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st) {
+  const int64_t nblk = (a.S + kTB - 1) / kTB;
+  route_scan_kernel<<<1, kScanThreads, 0, st>>>(nblk, a.S, a.E, a.k, a.cap, a.hist, a.psum,
+                                                a.first_cnt, a.routed, a.kept, a.offsets, a.l_aux);
+  const int64_t n = a.S * a.k;
+  if (n > 0) {
+    route_assign_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
+        a.S, a.E, a.k, a.cap, nblk, a.idx, a.hist, a.first_cnt, a.offsets, a.slot, a.row_src);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const int64_t nblk = (a.S + kTB - 1) / kTB;
   if (nblk > 0) {
     route_topk_kernel<<<unsigned(nblk), kTB, 0, st>>>(a.logits, a.S, a.E, a.k, a.probs,
                                                      a.idx, a.w, a.slot, a.hist, a.psum);
   }
-  route_scan_kernel<<<1, 512, 0, st>>>(nblk, a.S, a.E, a.k, a.cap, a.hist, a.psum,
-                                       a.first_cnt, a.routed, a.kept, a.offsets, a.l_aux);
-  const int64_t n = a.S * a.k;
-  if (n > 0) {
-    route_assign_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
-        a.S, a.E, a.k, a.cap, a.idx, a.hist, a.first_cnt, a.offsets, a.slot, a.row_src);
-  }
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_route_finish(a, st);
 }
 
 }  // namespace moe
