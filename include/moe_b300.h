@@ -144,6 +144,32 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x,
                          int32_t *row_src, float *l_aux, void *workspace,
                          size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_gate_topk without a workspace argument, for callers that cannot
+ * allocate device memory: code that is handed only its input and output
+ * buffers and a stream (a plugin inside another engine, a server that
+ * forbids allocation after start-up) and so cannot supply the scratch
+ * moe_gate_topk needs.  The pages have no counterpart to this entry point.
+ * Same arguments, outputs and results as moe_gate_topk; the caller still
+ * passes every input and output.  The scratch is a 16 MiB array compiled
+ * into the library, held by every GPU that loads the library until the
+ * process exits.  Configurations whose moe_workspace_size(cfg, 0) exceeds
+ * 16 MiB (about S*E > 4.1 million) are rejected with MOE_ERR_WORKSPACE
+ * before anything is enqueued.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call.  All calls on a device
+ * share the one array, so calls that can overlap on the GPU (different
+ * streams, or different host threads) race and must be serialised by the
+ * caller; results never depend on what an earlier call left there. */
+moe_status moe_gate_topk_static(const moe_config *cfg, const void *x,
+                                const void *w_gate, const float *logit_bias,
+                                float *logits, float *probs,
+                                int32_t *topk_idx, float *topk_w,
+                                int32_t *slot, int32_t *routed_cnt,
+                                int32_t *kept_cnt, int32_t *expert_offsets,
+                                int32_t *row_src, float *l_aux,
+                                moe_stream_t stream);
+
 /* The routing half of moe_gate_topk, taking the logits as input instead of
  * computing them (the same kernels; used to check routing bit for bit
  * against a reference that is fed identical fp32 logits).

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_workspace_size": (c_int, [POINTER(MoeConfig), c_int, POINTER(c_size_t)]),
     "moe_gate_topk": (c_int, [POINTER(MoeConfig)] + [_P] * 14 + [c_size_t, _P]),
     "moe_route_from_logits": (c_int, [POINTER(MoeConfig)] + [_P] * 11 + [c_size_t, _P]),
+    "moe_gate_topk_static": (c_int, [POINTER(MoeConfig)] + [_P] * 13 + [_P]),
     "moe_dispatch": (c_int, [POINTER(MoeConfig)] + [_P] * 5 + [_P]),
     "moe_expert_ffn": (c_int, [POINTER(MoeConfig)] + [_P] * 9 + [_P]),
     "moe_combine": (c_int, [POINTER(MoeConfig)] + [_P] * 6 + [_P]),
@@ -148,6 +149,16 @@ def moe_gate_topk(cfg, x, w_gate, logit_bias, logits, probs, topk_idx, topk_w, s
         _ptr(topk_idx), _ptr(topk_w), _ptr(slot), _ptr(routed_cnt), _ptr(kept_cnt),
         _ptr(expert_offsets), _ptr(row_src), _ptr(l_aux), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_gate_topk_static(cfg, x, w_gate, logit_bias, logits, probs, topk_idx, topk_w, slot,
+                         routed_cnt, kept_cnt, expert_offsets, row_src, l_aux, stream=None):
+    """moe_gate_topk with no workspace argument (scratch compiled into the
+    library), for callers that cannot allocate device memory."""
+    _check("moe_gate_topk_static", _lib.moe_gate_topk_static(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(logits), _ptr(probs),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(slot), _ptr(routed_cnt), _ptr(kept_cnt),
+        _ptr(expert_offsets), _ptr(row_src), _ptr(l_aux), _stream(stream)))
 
 
 def moe_route_from_logits(cfg, logits, probs, topk_idx, topk_w, slot, routed_cnt, kept_cnt,
