@@ -354,7 +354,12 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
   MOE_CUDA(launch_combine_bwd(dy, sv->out_disp, dt, S, d, k, sv->topk_idx, sv->slot,
                               sv->expert_offsets, sv->topk_w, w.d_out, w.dw, st));
   // 2. dW2_e = dO_e^T h_e ; db2 = column sums of dO
-  {
+  if (dt == MOE_BF16) {
+    TcWgrad g{};
+    g.A = w.d_out; g.B = sv->h; g.rows_alloc = R > 0 ? R : 1; g.C = dw2;
+    g.M = d; g.N = f; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
+    MOE_CUDA(launch_tc_wgrad(g, st));
+  } else {
     SimtGemm g{};
     g.a_dtype = g.b_dtype = g.c_dtype = dt;
     g.A = w.d_out; g.a_m = 1; g.a_k = d;
@@ -385,7 +390,12 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     }
   }
   // 4. dW1_e = dh_pre_e^T x_disp_e ; db1 = column sums of dh_pre
-  {
+  if (dt == MOE_BF16) {
+    TcWgrad g{};
+    g.A = w.dh_pre; g.B = sv->x_disp; g.rows_alloc = R > 0 ? R : 1; g.C = dw1;
+    g.M = f; g.N = d; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
+    MOE_CUDA(launch_tc_wgrad(g, st));
+  } else {
     SimtGemm g{};
     g.a_dtype = g.b_dtype = g.c_dtype = dt;
     g.A = w.dh_pre; g.a_m = 1; g.a_k = f;

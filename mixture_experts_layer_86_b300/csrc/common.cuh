@@ -98,6 +98,10 @@ enum : uint32_t {
   kErrGateProducer = 0x05000000u,
   kErrGateMma = 0x06000000u,
   kErrGateEpilogue = 0x07000000u,
+  kErrWgradProducer = 0x08000000u,
+  kErrWgradMma = 0x09000000u,
+  kErrWgradEpilogue = 0x0a000000u,
+  kErrWgradFixup = 0x0b000000u,
 };
 
 __device__ __forceinline__ void record_error(unsigned int *err, uint32_t code) {

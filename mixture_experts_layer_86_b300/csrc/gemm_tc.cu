@@ -309,6 +309,267 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// ------------------------------------------------ K-grouped weight gradient
+// C_g[m, n] = sum over rows r of group g of A[r, m] * B[r, n]: the expert
+// weight gradients dW2_e = dO_e^T h_e and dW1_e = dh_pre_e^T x_disp_e, whose
+// reduction runs over the expert's (variable, possibly zero) token rows.
+// Both operands are MN-major in shared memory.  The last K block of a group
+// may hold rows of the next group (or unwritten rows past the last group):
+// a fixup warp zeroes those rows in shared memory before the MMA reads the
+// stage, so every K block goes producer -> full -> fixup -> ready -> MMA.
+// An expert with no rows gets an exact zero tile without touching TMEM.
+constexpr int kWgThreads = 224;  // + warp 6: fixup
+
+struct __align__(8) WgCtl {
+  uint64_t full[STAGES];
+  uint64_t ready[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kWgSmemBytes = 1024 + STAGES * (kABytes + kBBytes) + sizeof(WgCtl);
+
+__device__ __forceinline__ void wg_tile(int t, int mt, int nt, int &g, int &m, int &n) {
+  const int per = mt * nt;
+  g = t / per;
+  const int l = t - g * per;
+  n = l / mt;
+  m = l - n * mt;
+}
+
+__global__ void __launch_bounds__(kWgThreads, 1)
+tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const int32_t *__restrict__ offsets, int G, int M, int N,
+                __nv_bfloat16 *__restrict__ C, unsigned int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * kABytes;
+  WgCtl &ctl = *reinterpret_cast<WgCtl *>(smem + STAGES * (kABytes + kBBytes));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;
+  const int total = G * mt * nt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 128);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int *abort = &ctl.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int g, m, n;
+        wg_tile(t, mt, nt, g, m, n);
+        const int r0 = offsets[g], rows = offsets[g + 1] - r0;
+        const int nk = (rows + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kWaitLimitNs)) {
+            record_error(err, kErrWgradProducer | uint32_t(t & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, kABytes + kBBytes);
+          const int row = r0 + kb * BK;
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j)
+            ptx::tma_load_2d(ptx::smem_addr(sA + stage * kABytes + j * (BK * 128)), &tmA, fb,
+                             m * BM + j * 64, row);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes + j * (BK * 128)), &tmB, fb,
+                             n * BN + j * 64, row);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s))
+            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+                           kWaitLimitNs / 4);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------- fixup: zero rows past the group
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int g, m, n;
+      wg_tile(t, mt, nt, g, m, n);
+      const int rows = offsets[g + 1] - offsets[g];
+      const int nk = (rows + BK - 1) / BK;
+      for (int kb = 0; kb < nk; ++kb) {
+        bool got = true;
+        if (lane == 0)
+          got = ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs);
+        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          if (lane == 0) {
+            record_error(err, kErrWgradFixup | uint32_t(t & 0xffffff));
+            *abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        const int valid = rows - kb * BK;
+        if (valid < BK) {
+          const int nbytes = (BK - valid) * 128;  // contiguous tail of each 64-row box
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int box = 0; box < BM / 64 + BN / 64; ++box) {
+            uint8_t *base = box < BM / 64
+                                ? sA + stage * kABytes + box * (BK * 128)
+                                : sB + stage * kBBytes + (box - BM / 64) * (BK * 128);
+            for (int i = lane * 16; i < nbytes; i += 32 * 16)
+              *reinterpret_cast<uint4 *>(base + valid * 128 + i) = z;
+          }
+          ptx::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.ready[stage]));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, 1, 1);
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        int g, m, n;
+        wg_tile(t, mt, nt, g, m, n);
+        const int rows = offsets[g + 1] - offsets[g];
+        const int nk = (rows + BK - 1) / BK;
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort, kWaitLimitNs)) {
+          record_error(err, kErrWgradMma | 0x800000u | uint32_t(t & 0x7fffff));
+          *abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.ready[stage]), phase, abort, kWaitLimitNs)) {
+            record_error(err, kErrWgradMma | uint32_t(t & 0x7fffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_addr(sA + stage * kABytes);
+          const uint32_t b0 = ptx::smem_addr(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            ptx::mma_bf16(d_tmem, ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024),
+                          ptx::sdesc_sw128(b0 + kk * 16 * 128, BK * 128, 1024), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+          ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) ptx::mma_commit(ptx::smem_addr(&ctl.tfull[acc]));
+      }
+      ptx::mma_commit(ptx::smem_addr(&ctl.drain));
+      if (!ptx::mbar_wait(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
+        record_error(err, kErrGemmDrain);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int r_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      int g, m, n;
+      wg_tile(t, mt, nt, g, m, n);
+      const bool empty_group = offsets[g + 1] == offsets[g];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort, kWaitLimitNs)) {
+        record_error(err, kErrWgradEpilogue | uint32_t(t & 0xffffff));
+        *abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int row = m * BM + r_in_tile;
+      const bool valid = row < M;
+      __nv_bfloat16 *crow = C + (int64_t(g) * M + row) * N;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t raw[32];
+        if (!empty_group) {
+          ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) raw[i] = 0u;
+        }
+        const int n0 = n * BN + c * 32;
+        if (!valid || n0 >= N) continue;
+#pragma unroll
+        for (int v8 = 0; v8 < 4; ++v8) {
+          const int col = n0 + v8 * 8;
+          if (col >= N) break;
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
+          *reinterpret_cast<uint4 *>(crow + col) = pack_bf16x8(x);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_addr(&ctl.tempty[acc]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 // ----------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -344,6 +605,27 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
 }
 
 }  // namespace
+
+cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
+  if (g.G <= 0) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.A, uint64_t(g.M), uint64_t(g.rows_alloc), 64, BK) ||
+      !make_map(&tb, g.B, uint64_t(g.N), uint64_t(g.rows_alloc), 64, BK))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kWgSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = g.G * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  tc_wgrad_kernel<<<grid, kWgThreads, kWgSmemBytes, st>>>(
+      ta, tb, g.offsets, g.G, g.M, g.N, static_cast<__nv_bfloat16 *>(g.C), g.err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
   if (g.G <= 0 || g.G > kMaxGroups) return cudaErrorInvalidValue;
