@@ -86,10 +86,16 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 3.0:      # let nvidia-smi start reporting
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -105,6 +111,7 @@ class ClockSampler:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
                     rows.append(parts)
+        rows = rows[1:] if len(rows) > 1 else rows   # first sample predates the load
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
@@ -185,7 +192,6 @@ def run_gpu(args):
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
-    clocks = sampler.stop()
 
     # ---- per-stage times: the same kernels through the stage entry points
     n_ev = 5
@@ -210,6 +216,8 @@ def run_gpu(args):
     torch.cuda.synchronize()
     stage_ms = {name: statistics.median(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
                 for j, name in enumerate(["gate", "dispatch", "expert_ffn", "combine"])}
+    clocks = sampler.stop()
+    train = train_step(args, dev, barrier, max_over_ranks, world)
 
     # ---- e2e: host buffers, copies inside the timed region
     x_host = inp_cpu.x.pin_memory()
@@ -265,7 +273,7 @@ def run_gpu(args):
         "combine": {"ms": stage_ms["combine"], "GB/s": gbs(comb_bytes, stage_ms["combine"]),
                     "frac_hbm": gbs(comb_bytes, stage_ms["combine"]) / hbm_peak},
     }
-    launches_per_step = 8  # gate GEMM, route x3, dispatch, 2 expert GEMMs, combine
+    launches_per_step = 7  # gate, scan, assign, dispatch, 2 expert GEMMs, combine
     line = {
         "metric": METRIC,
         "value": world * S * args.steps / (ms * 1e-3),
@@ -293,6 +301,7 @@ def run_gpu(args):
                      "launch_ms": gemm_launch_ms,
                      "traffic": traffic},
         "stages": stages,
+        "train_step": train,
         "e2e": {"value": world * S * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": S * dm * eb,
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
@@ -304,6 +313,67 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def train_step(args, dev, barrier, max_over_ranks, world):
+    """Forward + backward of the 32-expert training layer."""
+    import torch
+
+    from mixture_experts_layer_86_b300 import _native as N
+    from mixture_experts_layer_86_b300 import layer as L
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+
+    wl = WORKLOADS["train_e32"]
+    cfg = N.config_from_workload(wl)
+    d = make_inputs(wl).to(dev)
+    bufs = L.alloc_buffers(cfg, dev, training=True)
+    ws = L.alloc_workspace(cfg, dev)
+    wsb = L.alloc_workspace(cfg, dev, for_backward=True)
+    y = torch.empty_like(d.x)
+    grads = {"dx": torch.empty_like(d.x), "dw_gate": torch.empty_like(d.w_gate),
+             "dw1": torch.empty_like(d.w1), "db1": torch.empty_like(d.b1),
+             "dw2": torch.empty_like(d.w2), "db2": torch.empty_like(d.b2)}
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    fw, bw = [], []
+
+    def step(timed):
+        if timed:
+            ev[0].record(st)
+        N.moe_forward(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, y, bufs, ws, st)
+        if timed:
+            ev[1].record(st)
+        N.moe_backward(cfg, d.x, d.w_gate, d.w1, d.w2, bufs, d.dy, grads["dx"], grads["dw_gate"],
+                       grads["dw1"], grads["db1"], grads["dw2"], grads["db2"], wsb, st)
+        if timed:
+            ev[2].record(st)
+
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+    torch.cuda.synchronize()
+    R = int(bufs["expert_offsets"][-1].item())
+    steps = max(1, min(args.steps, 100))
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        step(False)
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    for _ in range(5):
+        step(True)
+        torch.cuda.synchronize()
+        fw.append(ev[0].elapsed_time(ev[1]))
+        bw.append(ev[1].elapsed_time(ev[2]))
+    flops = 12.0 * R * wl.hidden_size * wl.ffn_size   # expert GEMMs: 4 fwd + 8 bwd
+    return {"workload": workload_desc(wl).replace("forward", "forward+backward"),
+            "value": world * wl.num_tokens * steps / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
+            "fwd_ms": statistics.median(fw), "bwd_ms": statistics.median(bw),
+            "expert_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
 
 
 # ------------------------------------------------------------------- CPU oracle
@@ -338,17 +408,18 @@ def _blas_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, inp_cpu, args, budget_s: float = 15.0):
-    """The oracle, as it stands, on the first n tokens of the same workload,
-    n chosen from a short probe so the timed run takes about budget_s."""
+def cpu_baseline(wl, inp_cpu, args, budget_s: float = 12.0):
+    """The oracle, as it stands, on the first n tokens of the same workload;
+    n grows until one run takes at least budget_s (or covers the batch)."""
     _prepare_oracle_weights(inp_cpu)
-    t0 = time.perf_counter()
-    _oracle_forward_tokens(wl, inp_cpu, 64)
-    per_tok = (time.perf_counter() - t0) / 64
-    n = int(min(wl.num_tokens, max(64, budget_s / max(per_tok, 1e-9))))
-    t0 = time.perf_counter()
-    _oracle_forward_tokens(wl, inp_cpu, n)
-    dt = time.perf_counter() - t0
+    n = 64
+    while True:
+        t0 = time.perf_counter()
+        _oracle_forward_tokens(wl, inp_cpu, n)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= wl.num_tokens:
+            break
+        n = min(wl.num_tokens, int(n * max(1.5, min(8.0, 1.2 * budget_s / max(dt, 1e-3)))))
     return {"value": n / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
             "sample": f"float64 oracle forward on the first {n} of {wl.num_tokens} tokens "
                       f"(same layer, capacity recomputed for the sample), {dt:.1f} s"}

@@ -76,18 +76,20 @@ size_t fwd_ws_bytes(const moe_config *c) {
 
 struct BwdWs {
   void *d_out, *dh_pre, *dx_disp;
-  float *dw, *dlogits;
+  float *dw, *dlogits, *gate_partial;
   int32_t *first;
 };
 
 size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const int64_t R = max_rows_of(c);
   const size_t eb = elem_bytes(c->dtype);
-  const size_t sz[6] = {align256(size_t(R) * c->hidden_size * eb),
+  const size_t sz[7] = {align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(c->num_tokens) * c->k * 4),
                         align256(size_t(c->num_tokens) * c->num_experts * 4),
+                        align256(gate_wgrad_partial_bytes(c->num_tokens, c->num_experts,
+                                                          c->hidden_size)),
                         align256(size_t(c->num_experts) * 4)};
   if (w) {
     char *p = static_cast<char *>(base);
@@ -96,9 +98,12 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->dx_disp = p; p += sz[2];
     w->dw = reinterpret_cast<float *>(p); p += sz[3];
     w->dlogits = reinterpret_cast<float *>(p); p += sz[4];
+    w->gate_partial = reinterpret_cast<float *>(p); p += sz[5];
     w->first = reinterpret_cast<int32_t *>(p);
   }
-  return sz[0] + sz[1] + sz[2] + sz[3] + sz[4] + sz[5];
+  size_t total = 0;
+  for (size_t v : sz) total += v;
+  return total;
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -429,15 +434,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
   MOE_CUDA(launch_first_count(sv->topk_idx, S, k, E, w.first, st));
   MOE_CUDA(launch_gate_bwd(sv->probs, sv->topk_idx, w.dw, w.first, S, E, k,
                            cfg->aux_loss_weight, w.dlogits, st));
-  {
-    SimtGemm g{};
-    g.a_dtype = MOE_F32; g.b_dtype = dt; g.c_dtype = dt;
-    g.A = w.dlogits; g.a_m = 1; g.a_k = E;
-    g.B = x; g.b_n = 1; g.b_k = d;
-    g.C = dw_gate; g.c_m = d; g.c_n = 1;
-    g.M = E; g.N = d; g.K = int(S); g.mode = 0; g.act = -1;
-    MOE_CUDA(launch_simt_gemm(g, st));
-  }
+  MOE_CUDA(launch_gate_wgrad(w.dlogits, x, dt, S, d, E, w.gate_partial, dw_gate, st));
   // 7. dX = sum_j dx_disp[row] + dlogits W_g
   return cuda_status(launch_dx_combine(w.dx_disp, w.dlogits, w_gate, dt, S, d, E, k,
                                        sv->topk_idx, sv->slot, sv->expert_offsets, dx, st));

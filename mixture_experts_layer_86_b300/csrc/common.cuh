@@ -56,6 +56,69 @@ __device__ __forceinline__ float act_grad(float z, int act) {
   return 0.5f * (1.0f + erff(z * 0.7071067811865476f)) + z * pdf;
 }
 
+// 16-byte vector of row elements and its conversion to / from fp32.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int kN = 4;
+  __device__ static void to_f32(const uint4 &u, float *o) {
+    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+    o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 from_f32(const float *v) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                      __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int kN = 8;
+  __device__ static void to_f32(const uint4 &u, float *o) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static uint4 from_f32(const float *v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Activation variants for bf16 epilogues: tanh from the hardware
+// tanh.approx.f32 instruction (relative error about 2^-11, well below the
+// bf16 rounding of the stored result).
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float act_fwd_fast(float z, int act) {
+  if (act == MOE_ACT_GELU_TANH) {
+    const float u = 0.7978845608028654f * fmaf(0.044715f * z, z * z, z);
+    const float hz = 0.5f * z;
+    return fmaf(hz, tanh_fast(u), hz);
+  }
+  return act_fwd(z, act);
+}
+
+__device__ __forceinline__ float act_grad_fast(float z, int act) {
+  if (act == MOE_ACT_GELU_TANH) {
+    const float z2 = z * z;
+    const float u = 0.7978845608028654f * fmaf(0.044715f * z, z2, z);
+    const float t = tanh_fast(u);
+    const float du = 0.7978845608028654f * fmaf(0.134145f, z2, 1.0f);
+    return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * du;
+  }
+  return act_grad(z, act);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);

@@ -13,40 +13,6 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 
-// 16-byte vector of row elements and its conversion to / from fp32.
-template <typename T> struct Vec;
-template <> struct Vec<float> {
-  static constexpr int kN = 4;
-  __device__ static void to_f32(const uint4 &u, float *o) {
-    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
-    o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
-  }
-  __device__ static uint4 from_f32(const float *v) {
-    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                      __float_as_uint(v[2]), __float_as_uint(v[3]));
-  }
-};
-template <> struct Vec<__nv_bfloat16> {
-  static constexpr int kN = 8;
-  __device__ static void to_f32(const uint4 &u, float *o) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o[2 * i] = __uint_as_float(w[i] << 16);
-      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-  __device__ static uint4 from_f32(const float *v) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-};
-
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -219,27 +185,6 @@ gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx
   }
 }
 
-// dx[s] = sum_j dx_disp[row(s,j)] + sum_e dlogits[s,e] * w_gate[e,:]
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-dx_combine_kernel(const void *__restrict__ dx_disp, const float *__restrict__ dlogits,
-                  const void *__restrict__ w_gate, int dtype, int64_t S, int d, int E,
-                  int k, const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
-                  const int32_t *__restrict__ offsets, void *__restrict__ dx) {
-  const int lane = threadIdx.x & 31;
-  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
-  if (s >= S) return;
-  const int64_t r0 = row_of(idx, slot, offsets, s * k);
-  const int64_t r1 = k == 2 ? row_of(idx, slot, offsets, s * k + 1) : -1;
-  const float *dl = dlogits + s * E;
-  for (int c = lane; c < d; c += 32) {
-    float acc = 0.0f;
-    for (int e = 0; e < E; ++e) acc = fmaf(dl[e], load_elem(w_gate, dtype, int64_t(e) * d + c), acc);
-    if (r0 >= 0) acc += load_elem(dx_disp, dtype, r0 * d + c);
-    if (r1 >= 0) acc += load_elem(dx_disp, dtype, r1 * d + c);
-    store_elem(dx, dtype, s * d + c, acc);
-  }
-}
-
 inline unsigned token_blocks(int64_t S) { return unsigned((S + kWarpsPerCta - 1) / kWarpsPerCta); }
 
 }  // namespace
@@ -309,16 +254,6 @@ cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float 
   const float aux_scale = float(double(aux_w) * double(E) / (double(S) * double(S)));
   gate_bwd_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(probs, idx, dw, first, S, E, k,
                                                                  aux_scale, dlogits);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits, const void *w_gate,
-                              int dtype, int64_t S, int d, int E, int k, const int32_t *idx,
-                              const int32_t *slot, const int32_t *offsets, void *dx,
-                              cudaStream_t st) {
-  if (S == 0) return cudaSuccess;
-  dx_combine_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-      dx_disp, dlogits, w_gate, dtype, S, d, E, k, idx, slot, offsets, dx);
   return cudaGetLastError();
 }
 

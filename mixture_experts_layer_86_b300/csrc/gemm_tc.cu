@@ -284,13 +284,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (pre) *reinterpret_cast<uint4 *>(pre + ci) = pack_bf16x8(x);
           if (act >= 0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = act_fwd(x[i], act);
+            for (int i = 0; i < 8; ++i) x[i] = act_fwd_fast(x[i], act);
           }
           if (grad_src) {
             float z[8];
             unpack_bf16x8(*reinterpret_cast<const uint4 *>(grad_src + ci), z);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] *= act_grad(z[i], dact);
+            for (int i = 0; i < 8; ++i) x[i] *= act_grad_fast(z[i], dact);
           }
           *reinterpret_cast<uint4 *>(C + ci) = pack_bf16x8(x);
         }

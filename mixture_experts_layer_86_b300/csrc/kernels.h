@@ -141,6 +141,11 @@ cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx,
                             const float *dw, const int32_t *first, int64_t S,
                             int E, int k, float aux_w, float *dlogits,
                             cudaStream_t st);
+// dW_g = dlogits^T x: token-split fp32 partial sums, then a fixed-order sum.
+int64_t gate_wgrad_splits(int64_t S);
+size_t gate_wgrad_partial_bytes(int64_t S, int E, int d);
+cudaError_t launch_gate_wgrad(const float *dlogits, const void *x, int dtype, int64_t S, int d,
+                              int E, float *partial, void *dw_gate, cudaStream_t st);
 // dx[s] = sum_j dx_disp[row(s,j)] + dlogits[s] . w_gate
 cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits,
                               const void *w_gate, int dtype, int64_t S, int d,
