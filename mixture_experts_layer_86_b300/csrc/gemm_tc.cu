@@ -6,17 +6,27 @@
 // row counts live on the device (expert_offsets), so no host round trip is
 // needed between routing and the FFN.
 //
-// Tiling: 128 (rows) x 256 (n) output tile per CTA, K in 64-element (128 B)
-// slices, 4-stage TMA -> shared memory pipeline with 128-byte swizzle,
-// tcgen05.mma M=128 N=256 K=16 accumulating in TMEM, two TMEM accumulators
-// (2 x 256 columns) so the epilogue of one tile overlaps the MMAs of the
-// next.  Warp roles (192 threads):
+// Operand roles are swapped with respect to C = X W^T: the MMA computes
+// C^T = W X^T, so the expert's weights fill the 128-row M side and its
+// tokens are the N side.  N is a multiple of 16 chosen per tile, so an
+// expert's last token tile pads at most 15 rows instead of a 128-row M
+// tile's up to 127 -- at ~500 tokens per expert that padding was ~11% of
+// the tensor work.
+//
+// Tiling: 128 output features x up to 256 tokens per tile, K in 64-element
+// (128 B) slices, 4-stage TMA -> shared memory pipeline with 128-byte
+// swizzle, tcgen05.mma (M=128, N=16..256, K=16) accumulating in TMEM, two
+// TMEM accumulators (2 x 256 columns) so the epilogue of one tile overlaps
+// the MMAs of the next.  Warp roles (192 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM allocator + MMA issuer (one lane)
-//   warps 2..5  epilogue: tcgen05.ld -> bias / activation / dact -> bf16 ->
-//               global, rows masked to the expert's row block.
-// Tiles are ordered expert by expert, n-tile by n-tile, m fastest, so the
-// CTAs that run at the same time share weight tiles through L2.
+//   warps 2..5  epilogue: each owns 32 features (its TMEM lane quadrant);
+//               tcgen05.ld -> bias / activation / dact -> bf16, transposed
+//               through a 32 x 32 shared-memory stage so that token rows go
+//               out as 16-byte vectors, masked to the expert's tokens.
+// Tiles run expert by expert, token tile by token tile, feature tile
+// fastest, so CTAs running at the same time share the token tile in L2 and
+// an expert's weights stay in L2 across its token tiles.
 //
 // Every mbarrier wait is bounded: a wait that gives up records an error
 // code in the device error word, raises a CTA-wide abort flag, and the CTA
@@ -37,6 +47,9 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxGroups = kMaxExperts;
+// swapped-operand grouped GEMM: BM output features x up to BN tokens
+constexpr int kFeat = BM, kTok = BN;
+constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 tokens x 32 bf16 features
 
 struct __align__(8) SmemCtl {
   uint64_t full[STAGES];
@@ -46,18 +59,20 @@ struct __align__(8) SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int tile_start[kMaxGroups + 1];  // prefix of (m-tiles x n-tiles) over groups
+  int tile_start[kMaxGroups + 1];  // prefix of (token tiles x feature tiles) over groups
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * (kABytes + kBBytes) + sizeof(SmemCtl);
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * (kABytes + kBBytes) +
+                              4 * kStageBytesPerWarp + sizeof(SmemCtl);
 
 struct TileCoord {
-  int g, m, n, rows;  // group, m-tile, n-tile, rows of the group
-  int row0;           // first row of the group
+  int g, tt, ft;  // group, token tile, feature tile
+  int row0;       // first row of the group
+  int ntok;       // valid tokens of this tile (1..kTok)
 };
 
 __device__ __forceinline__ TileCoord tile_coord(const SmemCtl &c, const int32_t *offs, int G,
-                                                int nt, int t) {
+                                                int nf, int t) {
   int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -66,11 +81,12 @@ __device__ __forceinline__ TileCoord tile_coord(const SmemCtl &c, const int32_t 
   TileCoord tc;
   tc.g = lo;
   tc.row0 = offs[lo];
-  tc.rows = offs[lo + 1] - tc.row0;
-  const int mt = (tc.rows + BM - 1) / BM;
+  const int rows = offs[lo + 1] - tc.row0;
   const int local = t - c.tile_start[lo];
-  tc.n = local / mt;
-  tc.m = local - tc.n * mt;
+  tc.tt = local / nf;
+  tc.ft = local - tc.tt * nf;
+  const int left = rows - tc.tt * kTok;
+  tc.ntok = left < kTok ? left : kTok;
   return tc;
 }
 
@@ -92,9 +108,13 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <bool kBMN>
+// C[r, n] = epi( sum_k X[r, k] * W_g(n, k) ) for the rows r of group g.
+// kWMN: W_g is stored [K, N] (N contiguous, the dgrad case) instead of
+// [N, K].  The bf16 staging area of each epilogue warp is 32 token rows of
+// 32 features (64 B per row).
+template <bool kWMN>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                const int32_t *__restrict__ offsets, int G, int N, int K,
                const __nv_bfloat16 *__restrict__ bias, int act,
                __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
@@ -102,12 +122,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = smem + STAGES * kABytes;
-  SmemCtl &ctl = *reinterpret_cast<SmemCtl *>(smem + STAGES * (kABytes + kBBytes));
+  uint8_t *sA = smem;                                   // weights, 128 x 64 per stage
+  uint8_t *sB = smem + STAGES * kABytes;                // tokens, 256 x 64 per stage
+  uint8_t *sStage = smem + STAGES * (kABytes + kBBytes);
+  SmemCtl &ctl = *reinterpret_cast<SmemCtl *>(sStage + 4 * kStageBytesPerWarp);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = (N + BN - 1) / BN;
+  const int nf = (N + kFeat - 1) / kFeat;
   const int nk = (K + BK - 1) / BK;
 
   // ---------------------------------------------------------------- setup
@@ -125,15 +146,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int run = 0;
     for (int g = 0; g < G; ++g) {
       ctl.tile_start[g] = run;
-      run += ((offsets[g + 1] - offsets[g] + BM - 1) / BM) * nt;
+      run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
     }
     ctl.tile_start[G] = run;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tmA);
-    ptx::tma_prefetch_desc(&tmB);
+    ptx::tma_prefetch_desc(&tmW);
+    ptx::tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
@@ -155,8 +176,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t armed_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(ctl, offsets, G, nt, t);
-        const int arow = tc.row0 + tc.m * BM;
+        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const int xrow = tc.row0 + tc.tt * kTok;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kWaitLimitNs)) {
             record_error(err, kErrGemmProducer | uint32_t(t & 0xffffff));
@@ -166,17 +187,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
           ptx::mbar_arrive_expect_tx(fb, kABytes + kBBytes);
-          ptx::tma_load_2d(ptx::smem_addr(sA + stage * kABytes), &tmA, fb, kb * BK, arow);
-          if (!kBMN) {
-            ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes), &tmB, fb, kb * BK,
-                             tc.g * N + tc.n * BN);
+          if (!kWMN) {
+            ptx::tma_load_2d(ptx::smem_addr(sA + stage * kABytes), &tmW, fb, kb * BK,
+                             tc.g * N + tc.ft * kFeat);
           } else {
-            // four 64(n) x 64(k) boxes, 8 KB apart
+            // two 64(n) x 64(k) boxes, 8 KB apart
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes + j * (BK * 128)), &tmB, fb,
-                               tc.n * BN + j * 64, tc.g * K + kb * BK);
+            for (int j = 0; j < kFeat / 64; ++j)
+              ptx::tma_load_2d(ptx::smem_addr(sA + stage * kABytes + j * (BK * 128)), &tmW, fb,
+                               tc.ft * kFeat + j * 64, tc.g * K + kb * BK);
           }
+          ptx::tma_load_2d(ptx::smem_addr(sB + stage * kBBytes), &tmX, fb, kb * BK, xrow);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -196,12 +217,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, 0, kBMN ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const uint32_t idesc = ptx::idesc_bf16(kFeat, (tc.ntok + 15) & ~15, kWMN ? 1 : 0, 0);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort, kWaitLimitNs)) {
@@ -210,7 +232,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * kTok);
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs)) {
             record_error(err, kErrGemmMma | uint32_t(t & 0x7fffff));
@@ -223,9 +245,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t b0 = ptx::smem_addr(sB + stage * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = kBMN ? ptx::sdesc_sw128(b0 + kk * 16 * 128, BK * 128, 1024)
-                                     : ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
+            const uint64_t ad = kWMN ? ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024)
+                                     : ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
             ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
@@ -243,11 +265,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int r_in_tile = q * 32 + lane;
+    const int q = warp & 3;  // TMEM lane quadrant = this warp's 32 features
+    uint8_t *stg = sStage + q * kStageBytesPerWarp;
+    // the 16-byte piece (row tr, part) this lane moves in step `it` of a
+    // row copy: 8 rows of 64 B per step, 4 steps per 32-token chunk
+    const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(ctl, offsets, G, nt, t);
+      const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort, kWaitLimitNs)) {
@@ -256,43 +281,62 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         break;
       }
       ptx::tc_fence_after();
-      const int r = tc.m * BM + r_in_tile;
-      const bool valid = r < tc.rows;
-      const int64_t grow = int64_t(tc.row0) + r;
-      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+      const int f0 = tc.ft * kFeat + q * 32;  // first feature of this warp
+      const int f = f0 + lane;
+      float bv = 0.0f;
+      if (bias && f < N) bv = __bfloat162float(bias[int64_t(tc.g) * N + f]);
+      const int64_t tok0 = int64_t(tc.row0) + int64_t(tc.tt) * kTok;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * kTok);
+      const int nchunk = (tc.ntok + 31) >> 5;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < nchunk; ++c) {
         uint32_t raw[32];
         ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
         ptx::tmem_ld_wait();
-        const int n0 = tc.n * BN + c * 32;
-        if (!valid || n0 >= N) continue;
+        const int ntk = tc.ntok - c * 32 < 32 ? tc.ntok - c * 32 : 32;
+        const int64_t trow0 = tok0 + c * 32;
+        float x[32];
 #pragma unroll
-        for (int v8 = 0; v8 < 4; ++v8) {
-          const int n = n0 + v8 * 8;
-          if (n >= N) break;
-          float x[8];
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]) + bv;
+        if (grad_src) {
+          // act'(grad_src) for this warp's 32 x 32 block, rows in through the stage
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
-          if (bias) {
-            float b[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(bias + int64_t(tc.g) * N + n), b);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] += b[i];
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tr < ntk && fc < N)
+              v = *reinterpret_cast<const uint4 *>(grad_src + (trow0 + tr) * N + fc);
+            *reinterpret_cast<uint4 *>(stg + tr * 64 + pp * 16) = v;
           }
-          const int64_t ci = grow * N + n;
-          if (pre) *reinterpret_cast<uint4 *>(pre + ci) = pack_bf16x8(x);
-          if (act >= 0) {
+          __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = act_fwd_fast(x[i], act);
+          for (int i = 0; i < 32; ++i) {
+            const float z = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16 *>(stg + i * 64 + lane * 2));
+            x[i] *= act_grad_fast(z, dact);
           }
-          if (grad_src) {
-            float z[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(grad_src + ci), z);
+          __syncwarp();
+        }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] *= act_grad_fast(z[i], dact);
+        for (int pass = 0; pass < 2; ++pass) {
+          __nv_bfloat16 *dst = pass == 0 ? pre : C;
+          if (pass == 1 && act >= 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = act_fwd_fast(x[i], act);
           }
-          *reinterpret_cast<uint4 *>(C + ci) = pack_bf16x8(x);
+          if (dst == nullptr) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat16 *>(stg + i * 64 + lane * 2) = __float2bfloat16_rn(x[i]);
+          __syncwarp();
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
+            if (tr < ntk && fc < N)
+              *reinterpret_cast<uint4 *>(dst + (trow0 + tr) * N + fc) =
+                  *reinterpret_cast<const uint4 *>(stg + tr * 64 + pp * 16);
+          }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
@@ -629,15 +673,15 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
 
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
   if (g.G <= 0 || g.G > kMaxGroups) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, BM))
+  CUtensorMap tw, tx;
+  if (!make_map(&tx, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, kTok))
     return cudaErrorInvalidValue;
-  bool okb;
+  bool okw;
   if (g.b_kmajor)
-    okb = make_map(&tb, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, BN);
+    okw = make_map(&tw, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, kFeat);
   else
-    okb = make_map(&tb, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
-  if (!okb) return cudaErrorInvalidValue;
+    okw = make_map(&tw, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
+  if (!okw) return cudaErrorInvalidValue;
 
   static bool attr_set[2] = {false, false};
   const int which = g.b_kmajor ? 0 : 1;
@@ -650,7 +694,7 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
   }
   const int grid = num_sms();
   kern<<<grid, kThreads, kSmemBytes, st>>>(
-      ta, tb, g.offsets, g.G, g.N, g.K, static_cast<const __nv_bfloat16 *>(g.bias), g.act,
+      tw, tx, g.offsets, g.G, g.N, g.K, static_cast<const __nv_bfloat16 *>(g.bias), g.act,
       static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
       static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
   return cudaGetLastError();

@@ -25,8 +25,8 @@ struct RouteArgs {
   int32_t *row_src;     // [rows]
   float *l_aux;
   // workspace views
-  int32_t *hist;        // [k][E][nblk] per-CTA counts, then their scan
-  float *psum;          // [E][nblk] per-CTA probability sums
+  int32_t *hist;        // [nblk][k][E] per-CTA counts, then their scan
+  float *psum;          // [nblk][E] per-CTA probability sums
   int32_t *first_cnt;   // [E]
 };
 size_t route_workspace_bytes(int64_t S, int E, int k);

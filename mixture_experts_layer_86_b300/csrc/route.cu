@@ -13,8 +13,9 @@
 //     CTA, the rank of each token among the CTA's tokens with the same
 //     (j, e) (kept in `slot` for now), and the CTA's per-expert sum of
 //     probabilities.  Done by route_topk (fp32 logits in memory) or by the
-//     fused tensor-core gate (gate_tc.cu).  Counts are stored column-major,
-//     hist[(j*E + e)*nblk + cta], so each (j, e) column is contiguous.
+//     fused tensor-core gate (gate_tc.cu).  Counts are stored CTA-major,
+//     hist[(cta*k + j)*E + e], so a CTA writes one contiguous row and the
+//     scan reads rows with consecutive threads on consecutive columns.
 //  2. route_scan (one CTA): exclusive scan of every column over CTAs, in
 //     place; totals; routed / kept counts; offsets; l_aux.
 //  3. route_assign: slot = (first-choice total of e if j == 1) + scanned
@@ -148,7 +149,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
   for (int e = threadIdx.x; e < E; e += kTB) {
     float acc = 0.0f;
     for (int w = 0; w < kWarps; ++w) acc += s_psum[w][e];
-    psum[int64_t(e) * gridDim.x + blockIdx.x] = acc;
+    psum[int64_t(blockIdx.x) * E + e] = acc;
   }
 
   // ---- phase 2: one lane per token; rank among equal (j, e) in token order
@@ -169,7 +170,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
         s_wcnt[w][ee] = run;
         run += c;
       }
-      hist[(int64_t(j) * E + ee) * gridDim.x + blockIdx.x] = run;
+      hist[(int64_t(blockIdx.x) * k + j) * E + ee] = run;
     }
     __syncthreads();
     if (e >= 0 && s < S) rank_out[s * k + j] = s_wcnt[warp][e] + rank;
@@ -178,70 +179,112 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
 }
 
 constexpr int kScanThreads = 1024;
+constexpr int kScanMaxGroups = 32;
 
-// Exclusive scan of one contiguous column of n counts by one warp: lane l
-// owns blocks [l*per, (l+1)*per).  Returns the column total.
-__device__ int warp_scan_column(int32_t *col, int64_t n, int lane) {
-  const int64_t per = (n + 31) / 32;
-  const int64_t b0 = lane * per, b1 = min(n, b0 + per);
-  int local = 0;
-  for (int64_t b = b0; b < b1; ++b) local += col[b];
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFullMask, incl, o);
-    if (lane >= o) incl += t;
-  }
-  int run = incl - local;
-  for (int64_t b = b0; b < b1; ++b) {
-    const int c = col[b];
-    col[b] = run;
-    run += c;
-  }
-  return __shfl_sync(kFullMask, incl, 31);
-}
-
+// One CTA.  The per-CTA counts form an nblk x (k*E) row-major matrix; thread
+// t works on column t % ncol for a contiguous range of rows (group t / ncol),
+// so at every step consecutive threads touch consecutive words.  Group sums
+// go through shared memory, each group rewrites its rows with exclusive
+// prefixes, and the column totals give routed / kept counts, the expert
+// offsets (a warp scan) and l_aux.  Probability sums are added as 2^-30
+// fixed-point integers: exact, independent of the order, and clear of
+// B300's slow float64 pipe (a partial is at most the CTA's token count, so
+// S < 2^31 keeps every total below 2^61).
 __global__ void __launch_bounds__(kScanThreads)
 route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
                   int32_t *__restrict__ hist, const float *__restrict__ psum,
                   int32_t *__restrict__ first_cnt, int32_t *__restrict__ routed,
                   int32_t *__restrict__ kept, int32_t *__restrict__ offsets,
                   float *__restrict__ l_aux) {
+  __shared__ int32_t s_grp[kScanThreads];
+  __shared__ long long s_pgrp[kScanThreads];
   __shared__ int32_t s_tot[2][kMaxExperts];
   __shared__ double s_aux[kMaxExperts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kW = kScanThreads / 32;
-  for (int col = warp; col < k * E; col += kW) {
-    const int tot = warp_scan_column(hist + int64_t(col) * nblk, nblk, lane);
-    if (lane == 0) s_tot[col / E][col % E] = tot;
+  const int lane = threadIdx.x & 31;
+
+  // ---- count columns: exclusive scan over CTAs, in place
+  {
+    const int ncol = k * E;
+    const int G = min(kScanMaxGroups, kScanThreads / ncol);
+    const int col = threadIdx.x % ncol, g = threadIdx.x / ncol;
+    const bool act = g < G;
+    const int64_t per = (nblk + G - 1) / G;
+    const int64_t b0 = act ? min(nblk, g * per) : 0;
+    const int64_t b1 = act ? min(nblk, b0 + per) : 0;
+    int sum = 0;
+#pragma unroll 4
+    for (int64_t b = b0; b < b1; ++b) sum += hist[b * ncol + col];
+    if (act) s_grp[g * ncol + col] = sum;
+    __syncthreads();
+    if (act) {
+      int run = 0;
+      for (int gg = 0; gg < g; ++gg) run += s_grp[gg * ncol + col];
+#pragma unroll 4
+      for (int64_t b = b0; b < b1; ++b) {
+        const int v = hist[b * ncol + col];
+        hist[b * ncol + col] = run;
+        run += v;
+      }
+    }
+    if (threadIdx.x < ncol) {
+      int tot = 0;
+      for (int gg = 0; gg < G; ++gg) tot += s_grp[gg * ncol + threadIdx.x];
+      s_tot[threadIdx.x / E][threadIdx.x % E] = tot;
+    }
   }
-  for (int e = warp; e < E; e += kW) {
-    double ps = 0.0;
-    for (int64_t b = lane; b < nblk; b += 32) ps += double(psum[int64_t(e) * nblk + b]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(kFullMask, ps, o);
-    if (lane == 0) s_aux[e] = ps;
+  // ---- probability sums per expert
+  {
+    const int G = min(kScanMaxGroups, kScanThreads / E);
+    const int e = threadIdx.x % E, g = threadIdx.x / E;
+    const bool act = g < G;
+    const int64_t per = (nblk + G - 1) / G;
+    const int64_t b0 = act ? min(nblk, g * per) : 0;
+    const int64_t b1 = act ? min(nblk, b0 + per) : 0;
+    long long ps = 0;
+#pragma unroll 4
+    for (int64_t b = b0; b < b1; ++b) ps += __float2ll_rn(psum[b * E + e] * 1073741824.0f);
+    if (act) s_pgrp[g * E + e] = ps;
+    __syncthreads();
+    if (threadIdx.x < E) {
+      long long tot = 0;
+      for (int gg = 0; gg < G; ++gg) tot += s_pgrp[gg * E + threadIdx.x];
+      s_aux[threadIdx.x] = double(tot) * (1.0 / 1073741824.0);
+    }
   }
   __syncthreads();
-  const int t = threadIdx.x;
-  if (t < E) {
-    const int r = s_tot[0][t] + (k == 2 ? s_tot[1][t] : 0);
-    routed[t] = r;
-    kept[t] = (cap < 0 || r < cap) ? r : int(cap);
-    first_cnt[t] = s_tot[0][t];
-  }
-  if (t == 0) {
-    int run = 0;
+
+  // ---- counts, offsets and l_aux: warp 0, lane l owns experts [l*per, ...)
+  if (threadIdx.x < 32) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
     double aux = 0.0;
-    for (int e = 0; e < E; ++e) {
+    for (int e = e0; e < e1; ++e) {
+      const int r = s_tot[0][e] + (k == 2 ? s_tot[1][e] : 0);
+      const int kp = (cap < 0 || r < cap) ? r : int(cap);
+      routed[e] = r;
+      kept[e] = kp;
+      first_cnt[e] = s_tot[0][e];
+      local += kp;
+      aux += s_aux[e] * double(s_tot[0][e]);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
       offsets[e] = run;
       const int r = s_tot[0][e] + (k == 2 ? s_tot[1][e] : 0);
       run += (cap < 0 || r < cap) ? r : int(cap);
-      aux += s_aux[e] * double(s_tot[0][e]);
     }
-    offsets[E] = run;
+    if (lane == 31) offsets[E] = incl;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
     // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
-    *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
+    if (lane == 0) *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
   }
 }
 
@@ -258,7 +301,7 @@ __global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap, int64_
   const int j = int(i - s * k);
   const int e = idx[i];
   const int64_t b = s / kTB;
-  const int pos = hist[(int64_t(j) * E + e) * nblk + b] + (j == 1 ? first_cnt[e] : 0) + slot[i];
+  const int pos = hist[(b * k + j) * E + e] + (j == 1 ? first_cnt[e] : 0) + slot[i];
   if (cap < 0 || pos < cap) {
     slot[i] = pos;
     row_src[offsets[e] + pos] = int32_t(i);
