@@ -47,6 +47,7 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxGroups = kMaxExperts;
+constexpr int kMaxDevices = 64;
 // swapped-operand grouped GEMM: BM output features x up to BN tokens
 constexpr int kFeat = BM, kTok = BN;
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 tokens x 32 bf16 features
@@ -71,7 +72,8 @@ struct TileCoord {
   int ntok;       // valid tokens of this tile (1..kTok)
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const SmemCtl &c, const int32_t *offs, int G,
+template <typename Ctl>
+__device__ __forceinline__ TileCoord tile_coord(const Ctl &c, const int32_t *offs, int G,
                                                 int nf, int t) {
   int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t
   while (lo < hi) {
@@ -350,6 +352,287 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------ CTA-pair grouped GEMM
+// The same GEMM with tcgen05.mma.cta_group::2: a 2-CTA cluster computes a
+// 256-feature x (up to) 256-token tile as one M=256 MMA.  Each CTA loads
+// its own 128 weight rows and half of the token rows, so per K slice an SM
+// takes in 32 KB and its tensor core reads 8 KB of shared memory per MMA
+// instead of 12 KB: with one CTA per SM the 128 x 256 tile needs more
+// shared-memory bandwidth than the SM has, the pair does not.
+//   both CTAs   warp 0: TMA loads of this CTA's halves, completion counted
+//               on the even CTA's `full` barrier; warps 2..5: epilogue of
+//               this CTA's 128 features (its own TMEM), release of the
+//               accumulator on the even CTA's `tempty` barrier
+//   even CTA    warp 1: the pair's MMAs; commits are multicast to the
+//               `empty` / `tfull` barriers of both CTAs
+// TMEM is allocated and freed by warp 1 of both CTAs together.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairABytes = 128 * BK * 2;  // this CTA's 128 weight rows
+constexpr uint32_t kPairBBytes = 128 * BK * 2;  // this CTA's half of the tokens
+constexpr uint16_t kPairMask = 0x3;
+
+struct __align__(8) PairCtl {
+  uint64_t full[kPairStages];
+  uint64_t empty[kPairStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[kMaxGroups + 1];  // prefix of (token tiles x 256-feature tiles)
+};
+constexpr size_t kPairSmemBytes = 1024 + kPairStages * (kPairABytes + kPairBBytes) +
+                                  4 * kStageBytesPerWarp + sizeof(PairCtl);
+
+template <bool kWMN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmX,
+                    const int32_t *__restrict__ offsets, int G, int N, int K,
+                    const __nv_bfloat16 *__restrict__ bias, int act,
+                    __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
+                    const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kPairStages * kPairABytes;
+  uint8_t *sStage = smem + kPairStages * (kPairABytes + kPairBBytes);
+  PairCtl &ctl = *reinterpret_cast<PairCtl *>(sStage + 4 * kStageBytesPerWarp);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int nf = (N + 2 * kFeat - 1) / (2 * kFeat);
+  const int nk = (K + BK - 1) / BK;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 8);  // 4 epilogue warps x 2 CTAs
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    int run = 0;
+    for (int g = 0; g < G; ++g) {
+      ctl.tile_start[g] = run;
+      run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
+    }
+    ctl.tile_start[G] = run;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmW);
+    ptx::tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.tile_start[G];
+  volatile int *abort = &ctl.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const int half = ((tc.ntok + 15) & ~15) >> 1;  // token rows per CTA in the MMA
+        const int xrow = tc.row0 + tc.tt * kTok + int(rank) * half;
+        const int frow = tc.ft * 2 * kFeat + int(rank) * kFeat;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort,
+                                      kWaitLimitNs)) {
+            record_error(err, kErrGemmProducer | uint32_t(t & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = ptx::smem_addr(&ctl.full[stage]);
+          const uint32_t fb = ptx::mapa_shared(fb_local, 0);
+          if (rank == 0)
+            ptx::mbar_arrive_expect_tx(fb_local, 2 * (kPairABytes + kPairBBytes));
+          if (!kWMN) {
+            ptx::tma_load_2d_pair(ptx::smem_addr(sA + stage * kPairABytes), &tmW, fb, kb * BK,
+                                  tc.g * N + frow);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kFeat / 64; ++j)
+              ptx::tma_load_2d_pair(ptx::smem_addr(sA + stage * kPairABytes + j * (BK * 128)),
+                                    &tmW, fb, frow + j * 64, tc.g * K + kb * BK);
+          }
+          ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes), &tmX, fb, kb * BK, xrow);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every stage filled here is released by the pair's MMAs (and their
+      // arrivals on this CTA's barriers have landed) before the CTA moves on
+      for (int s = 0; s < kPairStages; ++s)
+        if (armed & (1u << s))
+          ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[s]), (armed_phase >> s) & 1u,
+                                 ok ? nullptr : abort, ok ? kWaitLimitNs : kWaitLimitNs / 4);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl, ++it) {
+        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const uint32_t idesc =
+            ptx::idesc_bf16(2 * kFeat, (tc.ntok + 15) & ~15, kWMN ? 1 : 0, 0);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort,
+                                    kWaitLimitNs)) {
+          record_error(err, kErrGemmMma | 0x800000u | uint32_t(t & 0x7fffff));
+          *abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * kTok);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.full[stage]), phase, abort,
+                                      kWaitLimitNs)) {
+            record_error(err, kErrGemmMma | uint32_t(t & 0x7fffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a0 = ptx::smem_addr(sA + stage * kPairABytes);
+          const uint32_t b0 = ptx::smem_addr(sB + stage * kPairBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = kWMN ? ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024)
+                                     : ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
+            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_mc(ptx::smem_addr(&ctl.empty[stage]), kPairMask);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) ptx::mma_commit_pair_mc(ptx::smem_addr(&ctl.tfull[acc]), kPairMask);
+      }
+      // every pair MMA has finished before either CTA frees TMEM
+      ptx::mma_commit_pair(ptx::smem_addr(&ctl.drain));
+      if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
+        record_error(err, kErrGemmDrain);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    uint8_t *stg = sStage + q * kStageBytesPerWarp;
+    const int pr = lane >> 2, pp = lane & 3;
+    int it = 0;
+    for (int t = cid; t < total; t += ncl, ++it) {
+      const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort,
+                                  kWaitLimitNs)) {
+        record_error(err, kErrGemmEpilogue | uint32_t(t & 0xffffff));
+        *abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int f0 = tc.ft * 2 * kFeat + int(rank) * kFeat + q * 32;
+      const int f = f0 + lane;
+      float bv = 0.0f;
+      if (bias && f < N) bv = __bfloat162float(bias[int64_t(tc.g) * N + f]);
+      const int64_t tok0 = int64_t(tc.row0) + int64_t(tc.tt) * kTok;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * kTok);
+      const int nchunk = (tc.ntok + 31) >> 5;
+#pragma unroll 1
+      for (int c = 0; c < nchunk; ++c) {
+        uint32_t raw[32];
+        ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
+        ptx::tmem_ld_wait();
+        const int ntk = tc.ntok - c * 32 < 32 ? tc.ntok - c * 32 : 32;
+        const int64_t trow0 = tok0 + c * 32;
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]) + bv;
+        if (grad_src) {
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tr < ntk && fc < N)
+              v = *reinterpret_cast<const uint4 *>(grad_src + (trow0 + tr) * N + fc);
+            *reinterpret_cast<uint4 *>(stg + tr * 64 + pp * 16) = v;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float z = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16 *>(stg + i * 64 + lane * 2));
+            x[i] *= act_grad_fast(z, dact);
+          }
+          __syncwarp();
+        }
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+          __nv_bfloat16 *dst = pass == 0 ? pre : C;
+          if (pass == 1 && act >= 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = act_fwd_fast(x[i], act);
+          }
+          if (dst == nullptr) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat16 *>(stg + i * 64 + lane * 2) = __float2bfloat16_rn(x[i]);
+          __syncwarp();
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
+            if (tr < ntk && fc < N)
+              *reinterpret_cast<uint4 *>(dst + (trow0 + tr) * N + fc) =
+                  *reinterpret_cast<const uint4 *>(stg + tr * 64 + pp * 16);
+          }
+          __syncwarp();
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa_shared(ptx::smem_addr(&ctl.tempty[acc]), 0));
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // the pair's MMAs, epilogues and remote arrivals are done
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -683,6 +966,49 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     okw = make_map(&tw, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
   if (!okw) return cudaErrorInvalidValue;
 
+  const int sms = num_sms();
+  if (sms >= 2) {
+    // CTA pairs: this CTA's weight rows (128) and half of the token tile
+    CUtensorMap txp;
+    if (!make_map(&txp, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, 128))
+      return cudaErrorInvalidValue;
+    const int which = g.b_kmajor ? 0 : 1;
+    auto kern = g.b_kmajor ? tc_gemm_pair_kernel<false> : tc_gemm_pair_kernel<true>;
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = kPairSmemBytes;
+    lc.stream = st;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    // persistent grid: as many pairs as can be resident at once
+    static int pairs[kMaxDevices][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (pairs[dev][which] == 0) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kPairSmemBytes));
+      if (e != cudaSuccess) return e;
+      lc.gridDim = dim3(sms & ~1);
+      int ncl = 0;
+      e = cudaOccupancyMaxActiveClusters(&ncl, kern, &lc);
+      if (e != cudaSuccess) return e;
+      if (ncl < 1) return cudaErrorInvalidConfiguration;
+      pairs[dev][which] = ncl < sms / 2 ? ncl : sms / 2;
+    }
+    lc.gridDim = dim3(2 * pairs[dev][which]);
+    return cudaLaunchKernelEx(&lc, kern, tw, txp, g.offsets, g.G, g.N, g.K,
+                              static_cast<const __nv_bfloat16 *>(g.bias), g.act,
+                              static_cast<__nv_bfloat16 *>(g.C),
+                              static_cast<__nv_bfloat16 *>(g.pre),
+                              static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
+  }
   static bool attr_set[2] = {false, false};
   const int which = g.b_kmajor ? 0 : 1;
   auto kern = g.b_kmajor ? tc_gemm_kernel<false> : tc_gemm_kernel<true>;
@@ -692,7 +1018,7 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[which] = true;
   }
-  const int grid = num_sms();
+  const int grid = sms;
   kern<<<grid, kThreads, kSmemBytes, st>>>(
       tw, tx, g.offsets, g.G, g.N, g.K, static_cast<const __nv_bfloat16 *>(g.bias), g.act,
       static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
