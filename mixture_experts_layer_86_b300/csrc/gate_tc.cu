@@ -147,6 +147,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      const uint64_t desc0 = ptx::sdesc_sw128(ptx::smem_addr(smem), 16, 1024);
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb) {
         const int stage = kb % nstages;
@@ -158,12 +159,11 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_addr(smem + stage * stage_bytes);
-        const uint32_t b0 = a0 + kGateABytes;
+        const uint64_t ast = ptx::sdesc_add(desc0, stage * stage_bytes);
+        const uint64_t bst = ptx::sdesc_add(ast, kGateABytes);
 #pragma unroll
         for (int kk = 0; kk < GBK / 16; ++kk)
-          ptx::mma_bf16(tmem, ptx::sdesc_sw128(a0 + kk * 32, 16, 1024),
-                        ptx::sdesc_sw128(b0 + kk * 32, 16, 1024), idesc,
+          ptx::mma_bf16(tmem, ptx::sdesc_add(ast, kk * 32), ptx::sdesc_add(bst, kk * 32), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
         ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
       }

@@ -61,6 +61,7 @@ struct __align__(8) SmemCtl {
   uint32_t tmem_base;
   int abort;
   int tile_start[kMaxGroups + 1];  // prefix of (token tiles x feature tiles) over groups
+  int row_start[kMaxGroups + 1];   // the expert offsets, read once from global memory
 };
 
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + STAGES * (kABytes + kBBytes) +
@@ -73,8 +74,7 @@ struct TileCoord {
 };
 
 template <typename Ctl>
-__device__ __forceinline__ TileCoord tile_coord(const Ctl &c, const int32_t *offs, int G,
-                                                int nf, int t) {
+__device__ __forceinline__ TileCoord tile_coord(const Ctl &c, int G, int nf, int t) {
   int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -82,8 +82,8 @@ __device__ __forceinline__ TileCoord tile_coord(const Ctl &c, const int32_t *off
   }
   TileCoord tc;
   tc.g = lo;
-  tc.row0 = offs[lo];
-  const int rows = offs[lo + 1] - tc.row0;
+  tc.row0 = c.row_start[lo];
+  const int rows = c.row_start[lo + 1] - tc.row0;
   const int local = t - c.tile_start[lo];
   tc.tt = local / nf;
   tc.ft = local - tc.tt * nf;
@@ -151,6 +151,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
     }
     ctl.tile_start[G] = run;
+    for (int g = 0; g <= G; ++g) ctl.row_start[g] = offsets[g];
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -178,7 +179,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
       uint32_t armed_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const TileCoord tc = tile_coord(ctl, G, nf, t);
         const int xrow = tc.row0 + tc.tt * kTok;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kWaitLimitNs)) {
@@ -219,12 +220,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      const uint64_t a_desc0 = kWMN ? ptx::sdesc_sw128(ptx::smem_addr(sA), BK * 128, 1024)
+                                    : ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
+      const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const TileCoord tc = tile_coord(ctl, G, nf, t);
         const uint32_t idesc = ptx::idesc_bf16(kFeat, (tc.ntok + 15) & ~15, kWMN ? 1 : 0, 0);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
@@ -243,15 +247,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_addr(sA + stage * kABytes);
-          const uint32_t b0 = ptx::smem_addr(sB + stage * kBBytes);
+          const uint64_t ast = ptx::sdesc_add(a_desc0, stage * kABytes);
+          const uint64_t bst = ptx::sdesc_add(b_desc0, stage * kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = kWMN ? ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024)
-                                     : ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            ptx::mma_bf16(d_tmem, ptx::sdesc_add(ast, kk * (kWMN ? 16 * 128 : 32)),
+                          ptx::sdesc_add(bst, kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
           if (++stage == STAGES) {
             stage = 0;
@@ -274,7 +275,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+      const TileCoord tc = tile_coord(ctl, G, nf, t);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort, kWaitLimitNs)) {
@@ -369,9 +370,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 //   even CTA    warp 1: the pair's MMAs; commits are multicast to the
 //               `empty` / `tfull` barriers of both CTAs
 // TMEM is allocated and freed by warp 1 of both CTAs together.
-constexpr int kPairStages = 6;
-constexpr uint32_t kPairABytes = 128 * BK * 2;  // this CTA's 128 weight rows
-constexpr uint32_t kPairBBytes = 128 * BK * 2;  // this CTA's half of the tokens
+constexpr int kPairKH = 2;                  // 64-wide K halves per stage
+constexpr int kPairBK = 64 * kPairKH;       // K per stage
+constexpr int kPairStages = 6 / kPairKH;
+constexpr uint32_t kHalfBytes = 128 * 64 * 2;           // 128 rows x 64 K, 16 KB
+constexpr uint32_t kPairABytes = kPairKH * kHalfBytes;  // this CTA's 128 weight rows
+constexpr uint32_t kPairBBytes = kPairKH * kHalfBytes;  // this CTA's half of the tokens
 constexpr uint16_t kPairMask = 0x3;
 
 struct __align__(8) PairCtl {
@@ -383,6 +387,7 @@ struct __align__(8) PairCtl {
   uint32_t tmem_base;
   int abort;
   int tile_start[kMaxGroups + 1];  // prefix of (token tiles x 256-feature tiles)
+  int row_start[kMaxGroups + 1];   // the expert offsets, read once from global memory
 };
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * (kPairABytes + kPairBBytes) +
                                   4 * kStageBytesPerWarp + sizeof(PairCtl);
@@ -407,7 +412,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   const uint32_t rank = ptx::cluster_ctarank();
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const int nf = (N + 2 * kFeat - 1) / (2 * kFeat);
-  const int nk = (K + BK - 1) / BK;
+  const int nk = (K + kPairBK - 1) / kPairBK;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -427,6 +432,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
     }
     ctl.tile_start[G] = run;
+    for (int g = 0; g <= G; ++g) ctl.row_start[g] = offsets[g];
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -453,7 +459,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       uint32_t phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl) {
-        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const TileCoord tc = tile_coord(ctl, G, nf, t);
         const int half = ((tc.ntok + 15) & ~15) >> 1;  // token rows per CTA in the MMA
         const int xrow = tc.row0 + tc.tt * kTok + int(rank) * half;
         const int frow = tc.ft * 2 * kFeat + int(rank) * kFeat;
@@ -469,16 +475,21 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
           const uint32_t fb = ptx::mapa_shared(fb_local, 0);
           if (rank == 0)
             ptx::mbar_arrive_expect_tx(fb_local, 2 * (kPairABytes + kPairBBytes));
-          if (!kWMN) {
-            ptx::tma_load_2d_pair(ptx::smem_addr(sA + stage * kPairABytes), &tmW, fb, kb * BK,
-                                  tc.g * N + frow);
-          } else {
 #pragma unroll
-            for (int j = 0; j < kFeat / 64; ++j)
-              ptx::tma_load_2d_pair(ptx::smem_addr(sA + stage * kPairABytes + j * (BK * 128)),
-                                    &tmW, fb, frow + j * 64, tc.g * K + kb * BK);
+          for (int h = 0; h < kPairKH; ++h) {
+            const int k0 = kb * kPairBK + h * 64;
+            uint8_t *a = sA + stage * kPairABytes + h * kHalfBytes;
+            if (!kWMN) {
+              ptx::tma_load_2d_pair(ptx::smem_addr(a), &tmW, fb, k0, tc.g * N + frow);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kFeat / 64; ++j)
+                ptx::tma_load_2d_pair(ptx::smem_addr(a + j * (64 * 128)), &tmW, fb, frow + j * 64,
+                                      tc.g * K + k0);
+            }
+            ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes + h * kHalfBytes), &tmX,
+                                  fb, k0, xrow);
           }
-          ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes), &tmX, fb, kb * BK, xrow);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kPairStages) {
@@ -497,12 +508,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   } else if (warp == 1) {
     // -------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
+      const uint64_t a_desc0 = kWMN ? ptx::sdesc_sw128(ptx::smem_addr(sA), BK * 128, 1024)
+                                    : ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
+      const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl, ++it) {
-        const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+        const TileCoord tc = tile_coord(ctl, G, nf, t);
         const uint32_t idesc =
             ptx::idesc_bf16(2 * kFeat, (tc.ntok + 15) & ~15, kWMN ? 1 : 0, 0);
         const int acc = it & 1;
@@ -524,14 +538,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_addr(sA + stage * kPairABytes);
-          const uint32_t b0 = ptx::smem_addr(sB + stage * kPairBBytes);
+          const uint64_t ast = ptx::sdesc_add(a_desc0, stage * kPairABytes);
+          const uint64_t bst = ptx::sdesc_add(b_desc0, stage * kPairBBytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = kWMN ? ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024)
-                                     : ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
-            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kPairBK / 16; ++kk) {
+            const uint32_t h = uint32_t(kk >> 2) * kHalfBytes, w = uint32_t(kk & 3);
+            ptx::mma_bf16_pair(d_tmem, ptx::sdesc_add(ast, h + w * (kWMN ? 16 * 128 : 32)),
+                               ptx::sdesc_add(bst, h + w * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&ctl.empty[stage]), kPairMask);
           if (++stage == kPairStages) {
@@ -553,7 +566,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
     for (int t = cid; t < total; t += ncl, ++it) {
-      const TileCoord tc = tile_coord(ctl, offsets, G, nf, t);
+      const TileCoord tc = tile_coord(ctl, G, nf, t);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort,
@@ -797,6 +810,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, 1, 1);
+      const uint64_t a_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sA), BK * 128, 1024);
+      const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), BK * 128, 1024);
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -822,13 +837,12 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a0 = ptx::smem_addr(sA + stage * kABytes);
-          const uint32_t b0 = ptx::smem_addr(sB + stage * kBBytes);
+          const uint64_t ast = ptx::sdesc_add(a_desc0, stage * kABytes);
+          const uint64_t bst = ptx::sdesc_add(b_desc0, stage * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            ptx::mma_bf16(d_tmem, ptx::sdesc_sw128(a0 + kk * 16 * 128, BK * 128, 1024),
-                          ptx::sdesc_sw128(b0 + kk * 16 * 128, BK * 128, 1024), idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+            ptx::mma_bf16(d_tmem, ptx::sdesc_add(ast, kk * 16 * 128),
+                          ptx::sdesc_add(bst, kk * 16 * 128), idesc, (kb | kk) != 0 ? 1u : 0u);
           ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
           if (++stage == STAGES) {
             stage = 0;

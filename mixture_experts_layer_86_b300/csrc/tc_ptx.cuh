@@ -148,6 +148,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the operand `off` bytes further on.  The start-address
+// field is the low 14 bits in 16-byte units and shared-memory addresses stay
+// below 256 KB, so the sum never carries out of the field; an MMA issue loop
+// then needs one add per operand instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t off) {
+  return desc + uint64_t(off >> 4);
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M x N tile,
 // A / B K-major (0) or MN-major (1).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

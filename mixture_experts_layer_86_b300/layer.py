@@ -71,3 +71,64 @@ def backward(cfg, x, w_gate, w1, w2, bufs, dy, workspace=None, grads=None, strea
     N.moe_backward(cfg, x, w_gate, w1, w2, bufs, dy, grads["dx"], grads["dw_gate"], grads["dw1"],
                    grads["db1"], grads["dw2"], grads["db2"], workspace, stream)
     return grads
+
+
+class HostPipeline:
+    """Forward passes over batches that live in (pinned) host memory, with the
+    host-to-device copy of the next batch and the device-to-host copy of the
+    previous result running on their own streams while the current forward
+    runs: two buffer slots, three streams, ordered by CUDA events.  This is
+    stream and buffer bookkeeping only; every step of the layer runs in the
+    library's kernels (``moe_forward``).
+
+    ``submit(x_host, y_host, laux_host=None, count_host=None)`` enqueues one
+    batch and returns at once; ``synchronize()`` waits for every result.  A
+    host output buffer may be reused once the submit that wrote it is two or
+    more calls back and its copy has finished (``synchronize``, or the
+    event returned by ``submit``)."""
+
+    def __init__(self, cfg, w_gate, logit_bias, w1, b1, w2, b2, device):
+        self.cfg = cfg
+        self.weights = (w_gate, logit_bias, w1, b1, w2, b2)
+        dt = torch_dtype(cfg)
+        shape = (cfg.num_tokens, cfg.hidden_size)
+        self.slots = [{"x": torch.empty(shape, dtype=dt, device=device),
+                       "y": torch.empty(shape, dtype=dt, device=device),
+                       "bufs": alloc_buffers(cfg, device),
+                       "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
+                       "ev_out": torch.cuda.Event(), "used": False} for _ in range(2)]
+        self.workspace = alloc_workspace(cfg, device)
+        self.s_in = torch.cuda.Stream(device)
+        self.s_comp = torch.cuda.Stream(device)
+        self.s_out = torch.cuda.Stream(device)
+        self.n = 0
+
+    def submit(self, x_host, y_host, laux_host=None, count_host=None):
+        sl = self.slots[self.n % 2]
+        if sl["used"]:
+            self.s_in.wait_event(sl["ev_comp"])      # the slot's last forward has read x
+        with torch.cuda.stream(self.s_in):
+            sl["x"].copy_(x_host, non_blocking=True)
+            sl["ev_in"].record(self.s_in)
+        self.s_comp.wait_event(sl["ev_in"])
+        if sl["used"]:
+            self.s_comp.wait_event(sl["ev_out"])     # the slot's last result is copied out
+        w_gate, logit_bias, w1, b1, w2, b2 = self.weights
+        N.moe_forward(self.cfg, sl["x"], w_gate, logit_bias, w1, b1, w2, b2, sl["y"],
+                      sl["bufs"], self.workspace, self.s_comp)
+        sl["ev_comp"].record(self.s_comp)
+        self.s_out.wait_event(sl["ev_comp"])
+        with torch.cuda.stream(self.s_out):
+            y_host.copy_(sl["y"], non_blocking=True)
+            if laux_host is not None:
+                laux_host.copy_(sl["bufs"]["l_aux"], non_blocking=True)
+            if count_host is not None:
+                count_host.copy_(sl["bufs"]["kept_cnt"], non_blocking=True)
+            sl["ev_out"].record(self.s_out)
+        sl["used"] = True
+        self.n += 1
+        return sl["ev_out"]
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()
