@@ -25,6 +25,7 @@ template <typename T>
 __global__ void __launch_bounds__(kGwThreads)
 gate_wgrad_partial_kernel(const float *__restrict__ dl, const T *__restrict__ x, int64_t S,
                           int d, int E, int64_t tok_per_split, float *__restrict__ partial) {
+  griddep_begin();
   __shared__ __align__(16) float s_dl[kGwK][kGwE];
   __shared__ __align__(16) float s_x[kGwK][kGwC];
   const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
@@ -86,6 +87,7 @@ gate_wgrad_partial_kernel(const float *__restrict__ dl, const T *__restrict__ x,
 // dW_g[e,c] = sum over splits, in split order
 __global__ void gate_wgrad_reduce_kernel(const float *__restrict__ partial, int nsplit, int E,
                                          int d, int dtype, void *__restrict__ dw_gate) {
+  griddep_begin();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= int64_t(E) * d) return;
   float acc = 0.0f;
@@ -105,6 +107,7 @@ dx_combine_tile_kernel(const T *__restrict__ dx_disp, const float *__restrict__ 
                        const T *__restrict__ w_gate, int64_t S, int d, int E, int k,
                        const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
                        const int32_t *__restrict__ offsets, T *__restrict__ dx) {
+  griddep_begin();
   __shared__ __align__(16) float s_dlT[kDxE][kDxT];
   __shared__ __align__(16) float s_w[kDxE][kDxC];
   __shared__ int64_t s_row[kDxT][2];
@@ -199,16 +202,16 @@ cudaError_t launch_gate_wgrad(const float *dlogits, const void *x, int dtype, in
   int64_t per = (S + nsplit - 1) / nsplit;
   if (per < 1) per = 1;
   dim3 grid((d + kGwC - 1) / kGwC, unsigned(nsplit), (E + kGwE - 1) / kGwE);
-  if (dtype == MOE_F32)
-    gate_wgrad_partial_kernel<float><<<grid, kGwThreads, 0, st>>>(
-        dlogits, static_cast<const float *>(x), S, d, E, per, partial);
-  else
-    gate_wgrad_partial_kernel<__nv_bfloat16><<<grid, kGwThreads, 0, st>>>(
-        dlogits, static_cast<const __nv_bfloat16 *>(x), S, d, E, per, partial);
+  const cudaError_t e =
+      dtype == MOE_F32
+          ? launch_k(gate_wgrad_partial_kernel<float>, grid, kGwThreads, 0, st, dlogits,
+                     static_cast<const float *>(x), S, d, E, per, partial)
+          : launch_k(gate_wgrad_partial_kernel<__nv_bfloat16>, grid, kGwThreads, 0, st, dlogits,
+                     static_cast<const __nv_bfloat16 *>(x), S, d, E, per, partial);
+  if (e != cudaSuccess) return e;
   const int64_t n = int64_t(E) * d;
-  gate_wgrad_reduce_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(partial, int(nsplit), E, d,
-                                                                      dtype, dw_gate);
-  return cudaGetLastError();
+  return launch_k(gate_wgrad_reduce_kernel, unsigned((n + 255) / 256), 256, 0, st, partial,
+                  int(nsplit), E, d, dtype, dw_gate);
 }
 
 cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits, const void *w_gate,
@@ -218,15 +221,13 @@ cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits, const v
   if (S == 0) return cudaSuccess;
   const dim3 grid((d + kDxC - 1) / kDxC, unsigned((S + kDxT - 1) / kDxT));
   if (dtype == MOE_F32)
-    dx_combine_tile_kernel<float><<<grid, kDxThreads, 0, st>>>(
-        static_cast<const float *>(dx_disp), dlogits, static_cast<const float *>(w_gate), S, d,
-        E, k, idx, slot, offsets, static_cast<float *>(dx));
-  else
-    dx_combine_tile_kernel<__nv_bfloat16><<<grid, kDxThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(dx_disp), dlogits,
-        static_cast<const __nv_bfloat16 *>(w_gate), S, d, E, k, idx, slot, offsets,
-        static_cast<__nv_bfloat16 *>(dx));
-  return cudaGetLastError();
+    return launch_k(dx_combine_tile_kernel<float>, grid, kDxThreads, 0, st,
+                    static_cast<const float *>(dx_disp), dlogits, static_cast<const float *>(w_gate),
+                    S, d, E, k, idx, slot, offsets, static_cast<float *>(dx));
+  return launch_k(dx_combine_tile_kernel<__nv_bfloat16>, grid, kDxThreads, 0, st,
+                  static_cast<const __nv_bfloat16 *>(dx_disp), dlogits,
+                  static_cast<const __nv_bfloat16 *>(w_gate), S, d, E, k, idx, slot, offsets,
+                  static_cast<__nv_bfloat16 *>(dx));
 }
 
 }  // namespace moe

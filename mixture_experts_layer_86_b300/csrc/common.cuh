@@ -119,6 +119,43 @@ __device__ __forceinline__ float act_grad_fast(float z, int act) {
   return act_grad(z, act);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with launch_k (below), so it may be scheduled while the previous kernel in
+// the stream is still finishing; it starts with griddep_begin(), which waits
+// until that kernel has completed and its writes are visible, and then lets
+// the next kernel be scheduled in turn.  The launch latency of each kernel
+// thereby overlaps the tail of the one before it.
+__device__ __forceinline__ void griddep_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, static_cast<KArgs>(args)...);
+}
+
+// Block barrier for code where lanes of a warp may have diverged (one lane
+// issuing TMA copies or MMAs in a loop, one lane polling a flag).
+// __syncthreads() is an aligned barrier: a warp counts as arrived as soon as
+// its first lanes reach it, so a lane still inside such a loop would be left
+// behind.  __syncwarp() waits for every lane of the warp first.
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);

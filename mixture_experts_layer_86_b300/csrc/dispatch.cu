@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 dispatch_kernel(const uint4 *__restrict__ x, int64_t S, int nvec, int k,
                 const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
                 const int32_t *__restrict__ offsets, uint4 *__restrict__ x_disp) {
+  griddep_begin();
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
   if (s >= S) return;
@@ -54,6 +55,7 @@ combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
                const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
                const int32_t *__restrict__ offsets, const float *__restrict__ w,
                uint4 *__restrict__ y) {
+  griddep_begin();
   using V = Vec<T>;
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
@@ -88,6 +90,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
                    const int32_t *__restrict__ slot, const int32_t *__restrict__ offsets,
                    const float *__restrict__ w, uint4 *__restrict__ d_out,
                    float *__restrict__ dw) {
+  griddep_begin();
   using V = Vec<T>;
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
@@ -120,6 +123,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
 __global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N,
                                     const int32_t *__restrict__ offsets,
                                     void *__restrict__ db) {
+  griddep_begin();
   __shared__ float part[8][33];
   const int g = blockIdx.y;
   const int n = blockIdx.x * 32 + threadIdx.x;
@@ -138,6 +142,7 @@ __global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N
 
 __global__ void first_count_kernel(const int32_t *__restrict__ idx, int64_t S, int k,
                                    int E, int32_t *__restrict__ first) {
+  griddep_begin();
   __shared__ int32_t cnt[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -151,6 +156,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx,
                 const float *__restrict__ dw, const int32_t *__restrict__ first,
                 int64_t S, int E, int k, float aux_scale, float *__restrict__ dlogits) {
+  griddep_begin();
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
   if (s >= S) return;
@@ -194,9 +200,9 @@ cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
                             void *x_disp, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
   const int nvec = d * elem_bytes(dtype) / 16;
-  dispatch_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-      static_cast<const uint4 *>(x), S, nvec, k, idx, slot, offsets, static_cast<uint4 *>(x_disp));
-  return cudaGetLastError();
+  return launch_k(dispatch_kernel, token_blocks(S), kWarpsPerCta * 32, 0, st,
+                  static_cast<const uint4 *>(x), S, nvec, k, idx, slot, offsets,
+                  static_cast<uint4 *>(x_disp));
 }
 
 cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d, int k,
@@ -205,14 +211,12 @@ cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d, in
   if (S == 0) return cudaSuccess;
   const int nvec = d * elem_bytes(dtype) / 16;
   if (dtype == MOE_F32)
-    combine_kernel<float><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-        static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-        static_cast<uint4 *>(y));
-  else
-    combine_kernel<__nv_bfloat16><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-        static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-        static_cast<uint4 *>(y));
-  return cudaGetLastError();
+    return launch_k(combine_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st,
+                    static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
+                    static_cast<uint4 *>(y));
+  return launch_k(combine_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st,
+                  static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
+                  static_cast<uint4 *>(y));
 }
 
 cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, int64_t S,
@@ -225,25 +229,21 @@ cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, 
   auto *o4 = static_cast<const uint4 *>(out_disp);
   auto *do4 = static_cast<uint4 *>(d_out);
   if (dtype == MOE_F32)
-    combine_bwd_kernel<float><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-        dy4, o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
-  else
-    combine_bwd_kernel<__nv_bfloat16><<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(
-        dy4, o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
-  return cudaGetLastError();
+    return launch_k(combine_bwd_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st, dy4, o4, S,
+                    nvec, k, idx, slot, offsets, w, do4, dw);
+  return launch_k(combine_bwd_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st, dy4,
+                  o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
 }
 
 cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
                                 const int32_t *offsets, void *db, cudaStream_t st) {
   dim3 grid((N + 31) / 32, G);
-  group_colsum_kernel<<<grid, dim3(32, 8), 0, st>>>(M, dtype, N, offsets, db);
-  return cudaGetLastError();
+  return launch_k(group_colsum_kernel, grid, dim3(32, 8), 0, st, M, dtype, N, offsets, db);
 }
 
 cudaError_t launch_first_count(const int32_t *idx, int64_t S, int k, int E, int32_t *first,
                                cudaStream_t st) {
-  first_count_kernel<<<1, 1024, 0, st>>>(idx, S, k, E, first);
-  return cudaGetLastError();
+  return launch_k(first_count_kernel, 1, 1024, 0, st, idx, S, k, E, first);
 }
 
 cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float *dw,
@@ -252,9 +252,8 @@ cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float 
   if (S == 0) return cudaSuccess;
   // d(aux_w * l_aux)/dp[s,e] = aux_w * E * first[e] / S^2
   const float aux_scale = float(double(aux_w) * double(E) / (double(S) * double(S)));
-  gate_bwd_kernel<<<token_blocks(S), kWarpsPerCta * 32, 0, st>>>(probs, idx, dw, first, S, E, k,
-                                                                 aux_scale, dlogits);
-  return cudaGetLastError();
+  return launch_k(gate_bwd_kernel, token_blocks(S), kWarpsPerCta * 32, 0, st, probs, idx, dw, first,
+                  S, E, k, aux_scale, dlogits);
 }
 
 }  // namespace moe

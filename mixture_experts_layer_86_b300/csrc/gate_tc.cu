@@ -83,6 +83,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                float *__restrict__ w_out, int32_t *__restrict__ rank_out,
                int32_t *__restrict__ hist, float *__restrict__ psum_out, int64_t nblk,
                unsigned int *err) {
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -113,7 +114,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort = &ctl.abort;
@@ -194,7 +195,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     ptx::tc_fence_before();
   }
-  __syncthreads();  // the logits tile is complete
+    block_sync();  // the logits tile is complete
 
   // ---- logits out: one token row (E floats) per warp step, coalesced
   if (logits_out)
@@ -232,7 +233,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   z += __shfl_xor_sync(kFullMask, z, 1);
   z += __shfl_xor_sync(kFullMask, z, 2);
   const float inv_z = 1.0f / z;
-  __syncthreads();  // every read of the logits tile is done
+    block_sync();  // every read of the logits tile is done
 
   // probabilities replace the logits in the tile (0 for tokens >= S)
   for (int e = c0; e < c1; ++e) trow_s[e] = valid ? expf(trow_s[e] - m) * inv_z : 0.0f;
@@ -253,7 +254,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     ctl.choice[0][tk] = valid ? i1 : -1;
     ctl.choice[1][tk] = (valid && k == 2) ? i2 : -1;
   }
-  __syncthreads();  // probabilities and choices are complete
+    block_sync();  // probabilities and choices are complete
 
   if (probs_out)
     for (int rr = warp; rr < GBM; rr += kGateThreads / 32)
@@ -302,7 +303,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, tmem_cols);
@@ -376,11 +377,9 @@ cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st) {
     attr_set = true;
   }
   const uint32_t idesc = ptx::idesc_bf16(GBM, E_pad, 0, 0);
-  gate_tc_kernel<<<unsigned(nblk), kGateThreads, smem, st>>>(
-      tx, tw, a.S, a.d, a.E, E_pad, a.k, idesc, cols, nstages, uint32_t(ring), a.logit_bias, a.logits, a.probs,
-      a.idx,
-      a.w, a.rank, a.hist, a.psum, nblk, a.err);
-  return cudaGetLastError();
+  return launch_k(gate_tc_kernel, unsigned(nblk), kGateThreads, smem, st, tx, tw, a.S, a.d, a.E,
+                  E_pad, a.k, idesc, cols, nstages, uint32_t(ring), a.logit_bias, a.logits, a.probs,
+                  a.idx, a.w, a.rank, a.hist, a.psum, nblk, a.err);
 }
 
 }  // namespace moe

@@ -12,6 +12,7 @@ namespace {
 constexpr int BM = 64, BN = 64, BK = 16;
 
 __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g) {
+  griddep_begin();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   __shared__ int s_group, s_row0, s_rows;
@@ -130,8 +131,7 @@ cudaError_t launch_simt_gemm(const SimtGemm &g, cudaStream_t st) {
     grid.z = g.mode == 2 ? g.G : 1;
   }
   if (grid.x == 0 || grid.y == 0 || grid.z == 0) return cudaSuccess;
-  simt_gemm_kernel<<<grid, 256, 0, st>>>(g);
-  return cudaGetLastError();
+  return launch_k(simt_gemm_kernel, grid, 256, 0, st, g);
 }
 
 }  // namespace moe

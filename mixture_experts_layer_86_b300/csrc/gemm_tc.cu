@@ -121,6 +121,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                const __nv_bfloat16 *__restrict__ bias, int act,
                __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -164,7 +165,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
   const int total = ctl.tile_start[G];
@@ -349,7 +350,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 
   // ------------------------------------------------------------- teardown
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -400,6 +401,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __nv_bfloat16 *__restrict__ bias, int act,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                     const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -445,7 +447,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
@@ -641,7 +643,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 
   // ------------------------------------------------------------- teardown
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   ptx::cluster_sync();  // the pair's MMAs, epilogues and remote arrivals are done
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -684,6 +686,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const int32_t *__restrict__ offsets, int G, int M, int N,
                 __nv_bfloat16 *__restrict__ C, unsigned int *err) {
+  griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -714,7 +717,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
   volatile int *abort = &ctl.abort;
@@ -904,7 +907,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+    block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -963,9 +966,8 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
   }
   const int tiles = g.G * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  tc_wgrad_kernel<<<grid, kWgThreads, kWgSmemBytes, st>>>(
-      ta, tb, g.offsets, g.G, g.M, g.N, static_cast<__nv_bfloat16 *>(g.C), g.err);
-  return cudaGetLastError();
+  return launch_k(tc_wgrad_kernel, grid, kWgThreads, kWgSmemBytes, st, ta, tb, g.offsets, g.G, g.M,
+                  g.N, static_cast<__nv_bfloat16 *>(g.C), g.err);
 }
 
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
@@ -1033,11 +1035,10 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     attr_set[which] = true;
   }
   const int grid = sms;
-  kern<<<grid, kThreads, kSmemBytes, st>>>(
-      tw, tx, g.offsets, g.G, g.N, g.K, static_cast<const __nv_bfloat16 *>(g.bias), g.act,
-      static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
-      static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
-  return cudaGetLastError();
+  return launch_k(kern, grid, kThreads, kSmemBytes, st, tw, tx, g.offsets, g.G, g.N, g.K,
+                  static_cast<const __nv_bfloat16 *>(g.bias), g.act,
+                  static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
+                  static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
 }
 
 }  // namespace moe

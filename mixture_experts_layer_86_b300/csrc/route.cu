@@ -38,6 +38,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
                   float *__restrict__ probs, int32_t *__restrict__ idx_out,
                   float *__restrict__ w_out, int32_t *__restrict__ rank_out,
                   int32_t *__restrict__ hist, float *__restrict__ psum) {
+  griddep_begin();
   __shared__ int32_t s_choice[2][kTB];
   __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
   __shared__ float s_psum[kWarps][kMaxExperts];
@@ -145,7 +146,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
     const int e = lane + 32 * q;
     if (q < nq && e < E) s_psum[warp][e] = pacc[q];
   }
-  __syncthreads();
+    block_sync();
   for (int e = threadIdx.x; e < E; e += kTB) {
     float acc = 0.0f;
     for (int w = 0; w < kWarps; ++w) acc += s_psum[w][e];
@@ -157,12 +158,12 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
   const int64_t s = tok0 + t;
   for (int j = 0; j < k; ++j) {
     for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += kTB) (&s_wcnt[0][0])[i] = 0;
-    __syncthreads();
+        block_sync();
     const int e = s_choice[j][t];
     const unsigned peers = __match_any_sync(kFullMask, e);
     const int rank = __popc(peers & lanemask_lt());
     if (e >= 0 && rank == 0) s_wcnt[warp][e] = __popc(peers);
-    __syncthreads();
+        block_sync();
     for (int ee = threadIdx.x; ee < E; ee += kTB) {
       int run = 0;
       for (int w = 0; w < kWarps; ++w) {
@@ -172,9 +173,9 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
       }
       hist[(int64_t(blockIdx.x) * k + j) * E + ee] = run;
     }
-    __syncthreads();
+        block_sync();
     if (e >= 0 && s < S) rank_out[s * k + j] = s_wcnt[warp][e] + rank;
-    __syncthreads();
+        block_sync();
   }
 }
 
@@ -196,6 +197,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
                   int32_t *__restrict__ first_cnt, int32_t *__restrict__ routed,
                   int32_t *__restrict__ kept, int32_t *__restrict__ offsets,
                   float *__restrict__ l_aux) {
+  griddep_begin();
   __shared__ int32_t s_grp[kScanThreads];
   __shared__ long long s_pgrp[kScanThreads];
   __shared__ int32_t s_tot[2][kMaxExperts];
@@ -215,7 +217,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
 #pragma unroll 4
     for (int64_t b = b0; b < b1; ++b) sum += hist[b * ncol + col];
     if (act) s_grp[g * ncol + col] = sum;
-    __syncthreads();
+        block_sync();
     if (act) {
       int run = 0;
       for (int gg = 0; gg < g; ++gg) run += s_grp[gg * ncol + col];
@@ -244,14 +246,14 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
 #pragma unroll 4
     for (int64_t b = b0; b < b1; ++b) ps += __float2ll_rn(psum[b * E + e] * 1073741824.0f);
     if (act) s_pgrp[g * E + e] = ps;
-    __syncthreads();
+        block_sync();
     if (threadIdx.x < E) {
       long long tot = 0;
       for (int gg = 0; gg < G; ++gg) tot += s_pgrp[gg * E + threadIdx.x];
       s_aux[threadIdx.x] = double(tot) * (1.0 / 1073741824.0);
     }
   }
-  __syncthreads();
+    block_sync();
 
   // ---- counts, offsets and l_aux: warp 0, lane l owns experts [l*per, ...)
   if (threadIdx.x < 32) {
@@ -295,6 +297,7 @@ __global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap, int64_
                                     const int32_t *__restrict__ offsets,
                                     int32_t *__restrict__ slot,
                                     int32_t *__restrict__ row_src) {
+  griddep_begin();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= S * k) return;
   const int64_t s = i / k;
@@ -330,12 +333,16 @@ void route_carve_workspace(RouteArgs &a, void *ws) {
 
 cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st) {
   const int64_t nblk = (a.S + kTB - 1) / kTB;
-  route_scan_kernel<<<1, kScanThreads, 0, st>>>(nblk, a.S, a.E, a.k, a.cap, a.hist, a.psum,
-                                                a.first_cnt, a.routed, a.kept, a.offsets, a.l_aux);
+  if (const cudaError_t e = launch_k(route_scan_kernel, 1, kScanThreads, 0, st, nblk, a.S, a.E, a.k,
+                                     a.cap, a.hist, a.psum, a.first_cnt, a.routed, a.kept, a.offsets,
+                                     a.l_aux); e != cudaSuccess)
+    return e;
   const int64_t n = a.S * a.k;
   if (n > 0) {
-    route_assign_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(
-        a.S, a.E, a.k, a.cap, nblk, a.idx, a.hist, a.first_cnt, a.offsets, a.slot, a.row_src);
+    if (const cudaError_t e = launch_k(route_assign_kernel, unsigned((n + 255) / 256), 256, 0, st,
+                                       a.S, a.E, a.k, a.cap, nblk, a.idx, a.hist, a.first_cnt,
+                                       a.offsets, a.slot, a.row_src); e != cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }
@@ -343,8 +350,10 @@ cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st) {
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const int64_t nblk = (a.S + kTB - 1) / kTB;
   if (nblk > 0) {
-    route_topk_kernel<<<unsigned(nblk), kTB, 0, st>>>(a.logits, a.S, a.E, a.k, a.probs,
-                                                     a.idx, a.w, a.slot, a.hist, a.psum);
+    if (const cudaError_t e = launch_k(route_topk_kernel, unsigned(nblk), kTB, 0, st, a.logits, a.S,
+                                       a.E, a.k, a.probs, a.idx, a.w, a.slot, a.hist,
+                                       a.psum); e != cudaSuccess)
+      return e;
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -100,3 +100,21 @@ def test_route_hand_worked_case():
     assert i64(out["kept_cnt"]).tolist() == [2, 2]
     assert i64(out["routed_cnt"]).tolist() == [4, 4]
     assert i64(out["expert_offsets"]).tolist() == [0, 2, 4]
+
+
+@pytest.mark.parametrize("S", [18000, 20000])
+def test_gate_routing_beyond_one_wave(S):
+    """The bf16 gate at d=2048 fits one 128-token CTA per SM: 18000 tokens
+    (141 CTAs, ragged last CTA) run in one wave on a 148-SM B300, 20000
+    tokens (157 CTAs) need a second.  Routing must match the oracle on the
+    GPU's own logits either way."""
+    wl = WORKLOADS["e8_bf16"].scaled(S)
+    wl = type(wl)(**{**wl.__dict__, "hidden_size": 2048, "ffn_size": 64, "name": f"gate_S{S}"})
+    run = GpuRun(wl, training=True)
+    g = run.oracle_route()
+    check_routing_equal(run, g)
+    b = run.bufs
+    assert np.allclose(f64(b["topk_w"]), g["weights"], rtol=2e-6, atol=1e-7)
+    assert np.allclose(f64(b["probs"]), g["probs"], rtol=2e-6, atol=1e-8)
+    assert abs(float(b["l_aux"].item()) - g["l_aux"]) <= 1e-5 * abs(g["l_aux"])
+    assert N.moe_get_device_error() == 0
