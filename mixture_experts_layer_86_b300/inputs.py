@@ -119,8 +119,27 @@ def make_inputs(wl: Workload, with_dy: Optional[bool] = None,
     dy = None
     if wl.backward if with_dy is None else with_dy:
         dy = draw((S, d), 1.0)
-    logit_bias = None
-    if wl.skew:
-        logit_bias = torch.tensor([wl.skew * math.log(1.0 / (e + 1)) for e in range(E)],
-                                  dtype=torch.float32)
-    return LayerInputs(x, w_gate, w1, b1, w2, b2, logit_bias, dy)
+    return LayerInputs(x, w_gate, w1, b1, w2, b2, skew_logit_bias(wl), dy)
+
+
+def skew_logit_bias(wl: Workload) -> Optional[torch.Tensor]:
+    """The skewed workload's per-expert logit bias b_e = skew * ln(1/(e+1))
+    (fp32), or None when the workload has no skew."""
+    if not wl.skew:
+        return None
+    return torch.tensor([wl.skew * math.log(1.0 / (e + 1)) for e in range(wl.num_experts)],
+                        dtype=torch.float32)
+
+
+def make_gate_inputs(wl: Workload):
+    """x, W_g and the logit bias exactly as make_inputs draws them (the first
+    two draws of the recipe), without drawing the expert weights."""
+    g = torch.Generator().manual_seed(wl.seed)
+    S, d, E = wl.num_tokens, wl.hidden_size, wl.num_experts
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(wl.torch_dtype)
+
+    x = draw((S, d), 1.0)
+    w_gate = draw((E, d), 1.0 / math.sqrt(d))
+    return x, w_gate, skew_logit_bias(wl)
