@@ -390,11 +390,15 @@ struct __align__(8) PairCtl {
   int tile_start[kMaxGroups + 1];  // prefix of (token tiles x 256-feature tiles)
   int row_start[kMaxGroups + 1];   // the expert offsets, read once from global memory
 };
+// 2 warps per TMEM lane quadrant take alternate 32-token chunks, so the
+// epilogue keeps up with tiles whose K loop is short (d = 512 or 1024)
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * (kPairABytes + kPairBBytes) +
-                                  4 * kStageBytesPerWarp + sizeof(PairCtl);
+                                  kPairEpiWarps * kStageBytesPerWarp + sizeof(PairCtl);
 
 template <bool kWMN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX,
                     const int32_t *__restrict__ offsets, int G, int N, int K,
@@ -408,7 +412,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   uint8_t *sA = smem;
   uint8_t *sB = smem + kPairStages * kPairABytes;
   uint8_t *sStage = smem + kPairStages * (kPairABytes + kPairBBytes);
-  PairCtl &ctl = *reinterpret_cast<PairCtl *>(sStage + 4 * kStageBytesPerWarp);
+  PairCtl &ctl = *reinterpret_cast<PairCtl *>(sStage + kPairEpiWarps * kStageBytesPerWarp);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -424,7 +428,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 8);  // 4 epilogue warps x 2 CTAs
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 2 * kPairEpiWarps);  // both CTAs
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
@@ -563,8 +567,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
-    uint8_t *stg = sStage + q * kStageBytesPerWarp;
+    const int q = warp & 3;             // TMEM lane quadrant = this warp's 32 features
+    const int half = (warp - 2) >> 2;   // which alternate 32-token chunks
+    uint8_t *stg = sStage + (warp - 2) * kStageBytesPerWarp;
     const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
     for (int t = cid; t < total; t += ncl, ++it) {
@@ -586,7 +591,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * kTok);
       const int nchunk = (tc.ntok + 31) >> 5;
 #pragma unroll 1
-      for (int c = 0; c < nchunk; ++c) {
+      for (int c = half; c < nchunk; c += 2) {
         uint32_t raw[32];
         ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
         ptx::tmem_ld_wait();
@@ -996,7 +1001,7 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    lc.blockDim = dim3(kThreads);
+    lc.blockDim = dim3(kPairThreads);
     lc.dynamicSmemBytes = kPairSmemBytes;
     lc.stream = st;
     lc.attrs = attr;
