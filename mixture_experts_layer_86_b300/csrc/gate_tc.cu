@@ -114,7 +114,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int *abort = &ctl.abort;
@@ -195,7 +195,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
     ptx::tc_fence_before();
   }
-    block_sync();  // the logits tile is complete
+  block_sync();  // the logits tile is complete
 
   // ---- logits out: one token row (E floats) per warp step, coalesced
   if (logits_out)
@@ -233,7 +233,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   z += __shfl_xor_sync(kFullMask, z, 1);
   z += __shfl_xor_sync(kFullMask, z, 2);
   const float inv_z = 1.0f / z;
-    block_sync();  // every read of the logits tile is done
+  block_sync();  // every read of the logits tile is done
 
   // probabilities replace the logits in the tile (0 for tokens >= S)
   for (int e = c0; e < c1; ++e) trow_s[e] = valid ? expf(trow_s[e] - m) * inv_z : 0.0f;
@@ -254,7 +254,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     ctl.choice[0][tk] = valid ? i1 : -1;
     ctl.choice[1][tk] = (valid && k == 2) ? i2 : -1;
   }
-    block_sync();  // probabilities and choices are complete
+  block_sync();  // probabilities and choices are complete
 
   if (probs_out)
     for (int rr = warp; rr < GBM; rr += kGateThreads / 32)
@@ -303,7 +303,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   }
 
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, tmem_cols);

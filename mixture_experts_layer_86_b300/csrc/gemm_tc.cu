@@ -165,7 +165,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
   const int total = ctl.tile_start[G];
@@ -350,7 +350,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 
   // ------------------------------------------------------------- teardown
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -451,7 +451,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
@@ -648,7 +648,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 
   // ------------------------------------------------------------- teardown
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   ptx::cluster_sync();  // the pair's MMAs, epilogues and remote arrivals are done
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -665,7 +665,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 // a fixup warp zeroes those rows in shared memory before the MMA reads the
 // stage, so every K block goes producer -> full -> fixup -> ready -> MMA.
 // An expert with no rows gets an exact zero tile without touching TMEM.
-constexpr int kWgThreads = 224;  // + warp 6: fixup
+// warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue (2 per TMEM lane
+// quadrant, alternate 32-column chunks: a tile's K loop is one expert's
+// tokens, short enough that 4 epilogue warps fell behind), 10 fixup
+constexpr int kWgEpiWarps = 8;
+constexpr int kWgFixupWarp = 2 + kWgEpiWarps;
+constexpr int kWgThreads = 32 * (kWgFixupWarp + 1);
 
 struct __align__(8) WgCtl {
   uint64_t full[STAGES];
@@ -710,7 +715,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 128);
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 32 * kWgEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
@@ -722,7 +727,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
   volatile int *abort = &ctl.abort;
@@ -770,7 +775,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
                            kWaitLimitNs / 4);
     }
-  } else if (warp == 6) {
+  } else if (warp == kWgFixupWarp) {
     // ------------------------------------- fixup: zero rows past the group
     int stage = 0;
     uint32_t phase = 0;
@@ -865,7 +870,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;             // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;   // which alternate 32-column chunks
     const int r_in_tile = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -885,7 +891,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       __nv_bfloat16 *crow = C + (int64_t(g) * M + row) * N;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = half; c < BN / 32; c += 2) {
         uint32_t raw[32];
         if (!empty_group) {
           ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
@@ -912,7 +918,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 
   ptx::tc_fence_before();
-    block_sync();
+  block_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);

@@ -146,7 +146,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
     const int e = lane + 32 * q;
     if (q < nq && e < E) s_psum[warp][e] = pacc[q];
   }
-    block_sync();
+  block_sync();
   for (int e = threadIdx.x; e < E; e += kTB) {
     float acc = 0.0f;
     for (int w = 0; w < kWarps; ++w) acc += s_psum[w][e];
@@ -158,12 +158,12 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
   const int64_t s = tok0 + t;
   for (int j = 0; j < k; ++j) {
     for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += kTB) (&s_wcnt[0][0])[i] = 0;
-        block_sync();
+    block_sync();
     const int e = s_choice[j][t];
     const unsigned peers = __match_any_sync(kFullMask, e);
     const int rank = __popc(peers & lanemask_lt());
     if (e >= 0 && rank == 0) s_wcnt[warp][e] = __popc(peers);
-        block_sync();
+    block_sync();
     for (int ee = threadIdx.x; ee < E; ee += kTB) {
       int run = 0;
       for (int w = 0; w < kWarps; ++w) {
@@ -173,9 +173,9 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
       }
       hist[(int64_t(blockIdx.x) * k + j) * E + ee] = run;
     }
-        block_sync();
+    block_sync();
     if (e >= 0 && s < S) rank_out[s * k + j] = s_wcnt[warp][e] + rank;
-        block_sync();
+    block_sync();
   }
 }
 
@@ -217,7 +217,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
 #pragma unroll 4
     for (int64_t b = b0; b < b1; ++b) sum += hist[b * ncol + col];
     if (act) s_grp[g * ncol + col] = sum;
-        block_sync();
+    block_sync();
     if (act) {
       int run = 0;
       for (int gg = 0; gg < g; ++gg) run += s_grp[gg * ncol + col];
@@ -246,14 +246,14 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
 #pragma unroll 4
     for (int64_t b = b0; b < b1; ++b) ps += __float2ll_rn(psum[b * E + e] * 1073741824.0f);
     if (act) s_pgrp[g * E + e] = ps;
-        block_sync();
+    block_sync();
     if (threadIdx.x < E) {
       long long tot = 0;
       for (int gg = 0; gg < G; ++gg) tot += s_pgrp[gg * E + threadIdx.x];
       s_aux[threadIdx.x] = double(tot) * (1.0 / 1073741824.0);
     }
   }
-    block_sync();
+  block_sync();
 
   // ---- counts, offsets and l_aux: warp 0, lane l owns experts [l*per, ...)
   if (threadIdx.x < 32) {
