@@ -229,6 +229,7 @@ def run_gpu(args):
     fwd_call_ms = max_over_ranks(e0.elapsed_time(e1))
     clocks = sampler.stop()
     train = train_step(args, dev, barrier, max_over_ranks, world)
+    decode = decode_step(args, dev, max_over_ranks, world)
 
     # ---- e2e: host buffers, copies inside the timed region.  Each step
     # copies its batch host -> device, runs moe_forward and copies y, l_aux
@@ -320,6 +321,7 @@ def run_gpu(args):
                                      "are unchanged, else null"},
         "stages": stages,
         "train_step": train,
+        "decode_step": decode,
         "e2e": {"value": world * S * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": S * dm * eb,
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
@@ -395,6 +397,70 @@ def train_step(args, dev, barrier, max_over_ranks, world):
             "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
             "fwd_ms": statistics.median(fw), "bwd_ms": statistics.median(bw),
             "expert_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
+
+
+def decode_step(args, dev, max_over_ranks, world):
+    """Inference shape: one decode step of 256 sequences through the 64-expert
+    layer.  Each expert sees a handful of tokens, so the expert GEMMs stream
+    the routed experts' weights: their roofline is HBM bandwidth."""
+    import torch
+
+    from mixture_experts_layer_86_b300 import _native as N
+    from mixture_experts_layer_86_b300 import layer as L
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+
+    wl = WORKLOADS["decode_e64"]
+    cfg = N.config_from_workload(wl)
+    d = make_inputs(wl).to(dev)
+    bufs = L.alloc_buffers(cfg, dev)
+    ws = L.alloc_workspace(cfg, dev)
+    y = torch.empty_like(d.x)
+    st = torch.cuda.current_stream()
+    steps = max(1, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+
+    def step(e=None):
+        if e is not None:
+            e[0].record(st)
+        N.moe_gate_topk(cfg, d.x, d.w_gate, d.logit_bias, bufs["logits"], None, bufs["topk_idx"],
+                        bufs["topk_w"], bufs["slot"], bufs["routed_cnt"], bufs["kept_cnt"],
+                        bufs["expert_offsets"], bufs["row_src"], bufs["l_aux"], ws, st)
+        N.moe_dispatch(cfg, d.x, bufs["topk_idx"], bufs["slot"], bufs["expert_offsets"],
+                       bufs["x_disp"], st)
+        if e is not None:
+            e[1].record(st)
+        N.moe_expert_ffn(cfg, bufs["x_disp"], bufs["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
+                         None, bufs["h"], bufs["out_disp"], st)
+        if e is not None:
+            e[2].record(st)
+        N.moe_combine(cfg, bufs["out_disp"], bufs["topk_idx"], bufs["slot"],
+                      bufs["expert_offsets"], bufs["topk_w"], y, st)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        step(ev[i])
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    ffn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    kept = bufs["kept_cnt"].cpu()
+    R = int(kept.sum())
+    dm, f = wl.hidden_size, wl.ffn_size
+    used = int((kept > 0).sum())
+    # algorithmic bytes of the two expert GEMMs: the weights (and biases) of
+    # every expert with a kept token, x_disp in, h out and back in, out_disp out
+    ffn_bytes = used * (2 * f * dm + f + dm) * 2 + R * (2 * dm + 2 * f) * 2
+    peaks, _ = load_peaks()
+    gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
+    return {"workload": workload_desc(wl), "value": world * wl.num_tokens * steps / (ms * 1e-3),
+            "unit": "tokens/s", "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
+            "experts_used": used,
+            "expert_ffn": {"ms": ffn_ms, "bytes": ffn_bytes, "GB/s": gbs, "bound": "hbm",
+                           "frac_hbm": gbs / peaks["hbm_gbs"]}}
 
 
 # ------------------------------------------------------------------- CPU oracle

@@ -55,7 +55,8 @@ class Workload:
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
 
 
-# The five layer configurations the implementation is specified and measured on.
+# The five layer configurations the implementation is specified and measured
+# on, and the inference (decode) shape of the 64-expert layer.
 WORKLOADS: Dict[str, Workload] = {
     # tiny fp32 forward, ReLU, k=1
     "tiny_fp32": Workload("tiny_fp32", 256, 32, 64, 4, 1, 1.0, 4, True,
@@ -75,6 +76,12 @@ WORKLOADS: Dict[str, Workload] = {
     "train_e32": Workload("train_e32", 8192, 1024, 4096, 32, 2, 1.25, 4, True,
                           "gelu_tanh", "bf16", seed=4, aux_loss_weight=0.01,
                           backward=True),
+    # inference: one decode step of 256 sequences through the 64-expert
+    # layer, with the evaluation capacity factor (1.0) as the capacity
+    # factor; every expert sees a handful of tokens, so the expert GEMMs
+    # stream the weights and are bound by HBM, not by the tensor cores
+    "decode_e64": Workload("decode_e64", 256, 2048, 5120, 64, 2, 1.0, 4, True,
+                           "gelu_tanh", "bf16", seed=5),
 }
 
 

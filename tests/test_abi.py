@@ -62,7 +62,8 @@ def test_capacity_matches_oracle():
 def test_layer_config_capacities():
     from mixture_experts_layer_86_b300.inputs import WORKLOADS
     want = {"tiny_fp32": 64, "e8_bf16": 1024, "e64_bf16": 640, "skew_e16_drop": 2048,
-            "skew_e16_nodrop": -1, "train_e32": 640}
+            "skew_e16_nodrop": -1, "train_e32": 640,
+            "decode_e64": 8}  # max(4, ceil(256*2*1.0/64))
     for name, wl in WORKLOADS.items():
         assert N.moe_capacity(N.config_from_workload(wl)) == want[name]
 

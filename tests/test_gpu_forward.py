@@ -16,7 +16,7 @@ from oracle import moe_oracle as O
 pytestmark = pytest.mark.gpu
 
 SMALL = [("tiny_fp32", 256), ("e8_bf16", 1000), ("e64_bf16", 300), ("skew_e16_drop", 700),
-         ("skew_e16_nodrop", 700), ("train_e32", 600)]
+         ("skew_e16_nodrop", 700), ("train_e32", 600), ("decode_e64", 256)]
 
 
 def _small(name, S):

@@ -14,7 +14,8 @@ from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
 
-FULL = ["tiny_fp32", "e8_bf16", "e64_bf16", "skew_e16_drop", "skew_e16_nodrop", "train_e32"]
+FULL = ["tiny_fp32", "e8_bf16", "e64_bf16", "skew_e16_drop", "skew_e16_nodrop", "train_e32",
+        "decode_e64"]
 
 
 @pytest.mark.parametrize("name", FULL)
