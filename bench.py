@@ -230,6 +230,7 @@ def run_gpu(args):
     clocks = sampler.stop()
     train = train_step(args, dev, barrier, max_over_ranks, world)
     decode = decode_step(args, dev, max_over_ranks, world)
+    residual = residual_step(args, dev, d, cfg, wl, max_over_ranks, world)
 
     # ---- e2e: host buffers, copies inside the timed region.  Each step
     # copies its batch host -> device, runs moe_forward and copies y, l_aux
@@ -322,6 +323,7 @@ def run_gpu(args):
         "stages": stages,
         "train_step": train,
         "decode_step": decode,
+        "residual_step": residual,
         "e2e": {"value": world * S * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": S * dm * eb,
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
@@ -397,6 +399,46 @@ def train_step(args, dev, barrier, max_over_ranks, world):
             "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
             "fwd_ms": statistics.median(fw), "bwd_ms": statistics.median(bw),
             "expert_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
+
+
+def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
+    """PR-MoE forward (moe_forward_residual: the layer plus a dense MLP of
+    one expert's shape on every token) on the same workload."""
+    import torch
+
+    from mixture_experts_layer_86_b300 import _native as N
+    from mixture_experts_layer_86_b300 import layer as L
+    from mixture_experts_layer_86_b300.inputs import make_residual_weights
+
+    rw = [t.to(dev) for t in make_residual_weights(wl)]
+    bufs = L.alloc_buffers(cfg, dev)
+    ws = L.alloc_workspace(cfg, dev)
+    y = torch.empty_like(d.x)
+    res_h = torch.empty((wl.num_tokens, wl.ffn_size), dtype=d.x.dtype, device=dev)
+    res_out = torch.empty_like(d.x)
+    st = torch.cuda.current_stream()
+
+    def step():
+        N.moe_forward_residual(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, *rw, y,
+                               bufs, res_h, res_out, ws, st)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    R = int(bufs["expert_offsets"][-1].item())
+    flops = 4.0 * (R + wl.num_tokens) * wl.hidden_size * wl.ffn_size
+    return {"workload": workload_desc(wl).replace("MoE layer forward", "PR-MoE forward (+ dense MLP)"),
+            "value": world * wl.num_tokens * steps / (ms * 1e-3), "unit": "tokens/s",
+            "ms_per_step": ms / steps, "steps": steps,
+            "expert_and_mlp_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
 
 
 def decode_step(args, dev, max_over_ranks, world):

@@ -224,6 +224,25 @@ moe_status moe_forward(const moe_config *cfg, const void *x,
                        void *workspace, size_t workspace_bytes,
                        moe_stream_t stream);
 
+/* The forward pass with PR-MoE's residual expert (deepspeed.moe overview
+ * §2.3 / §3.3, MoE(..., use_residual=True): "a fixed MLP combined with the
+ * dynamic experts").  The page gives no mixing formula; the residual
+ * connection is read as a sum:
+ *   y = MoE(x) + MLP(x),   MLP(x) = act(x rw1^T + rb1) rw2^T + rb2
+ * with the MLP (the same shape and activation as one expert) applied to
+ * every token.  rw1: [f,d]; rb1: [f]; rw2: [d,f]; rb2: [d] (T);
+ * res_h: [S,f] T and res_out: [S,d] T receive the MLP's activation and
+ * output (caller-owned scratch); the other arguments are moe_forward's.
+ * The MLP's output is added inside the combine, in fp32. */
+moe_status moe_forward_residual(const moe_config *cfg, const void *x,
+                                const void *w_gate, const float *logit_bias,
+                                const void *w1, const void *b1, const void *w2,
+                                const void *b2, const void *rw1, const void *rb1,
+                                const void *rw2, const void *rb2, void *y,
+                                const moe_buffers *buf, void *res_h, void *res_out,
+                                void *workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
 /* Backward of L = <dy, y> + aux_loss_weight * l_aux with the routing held
  * fixed (DeepSeek-MoE page §3.1 TopKRouter: the gradient reaches only the
  * selected logits; §2.1/§2.3: an expert that got no token has zero weight

@@ -178,6 +178,38 @@ moe_status expert_ffn(const moe_config *c, const void *x_disp, const int32_t *of
   return cuda_status(launch_simt_gemm(g2, st));
 }
 
+// The residual expert of PR-MoE on every token: h = act(x rw1^T + rb1),
+// out = h rw2^T + rb2 -- the grouped GEMM with one group of all S rows.
+moe_status dense_mlp(const moe_config *c, const void *x, const void *rw1, const void *rb1,
+                     const void *rw2, const void *rb2, void *h, void *out, cudaStream_t st) {
+  const int64_t S = c->num_tokens;
+  const int d = c->hidden_size, f = c->ffn_size;
+  if (S == 0) return MOE_OK;
+  if (c->dtype == MOE_BF16) {
+    TcGemm g1{};
+    g1.A = x; g1.rows_alloc = S; g1.B = rw1; g1.b_kmajor = true; g1.C = h;
+    g1.N = f; g1.K = d; g1.G = 1; g1.offsets = nullptr; g1.bias = rb1; g1.act = c->act;
+    g1.pre = nullptr; g1.grad_src = nullptr; g1.dact = 0; g1.err = device_error_ptr();
+    MOE_CUDA(launch_tc_gemm(g1, st));
+    TcGemm g2 = g1;
+    g2.A = h; g2.B = rw2; g2.C = out; g2.N = d; g2.K = f; g2.bias = rb2; g2.act = -1;
+    return cuda_status(launch_tc_gemm(g2, st));
+  }
+  SimtGemm g{};
+  g.a_dtype = g.b_dtype = g.c_dtype = c->dtype;
+  g.A = x; g.a_m = d; g.a_k = 1;
+  g.B = rw1; g.b_n = d; g.b_k = 1;
+  g.C = h; g.c_m = f; g.c_n = 1;
+  g.M = S; g.N = f; g.K = d; g.mode = 0; g.bias = rb1; g.act = c->act;
+  MOE_CUDA(launch_simt_gemm(g, st));
+  SimtGemm g2 = g;
+  g2.A = h; g2.a_m = f;
+  g2.B = rw2; g2.b_n = f;
+  g2.C = out; g2.c_m = d;
+  g2.N = d; g2.K = f; g2.bias = rb2; g2.act = -1;
+  return cuda_status(launch_simt_gemm(g2, st));
+}
+
 }  // namespace
 
 int num_sms() {
@@ -335,6 +367,32 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_gate,
   return cuda_status(launch_combine(buf->out_disp, cfg->dtype, cfg->num_tokens, cfg->hidden_size,
                                     cfg->k, buf->topk_idx, buf->slot, buf->expert_offsets,
                                     buf->topk_w, y, stream));
+}
+
+moe_status moe_forward_residual(const moe_config *cfg, const void *x, const void *w_gate,
+                                const float *logit_bias, const void *w1, const void *b1,
+                                const void *w2, const void *b2, const void *rw1, const void *rb1,
+                                const void *rw2, const void *rb2, void *y, const moe_buffers *buf,
+                                void *res_h, void *res_out, void *workspace,
+                                size_t workspace_bytes, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (!buf || !ok_ptr(y) || !ok_ptr(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
+      !ok_opt(buf->h_pre) || !ok_ptr(w1) || !ok_ptr(b1) || !ok_ptr(w2) || !ok_ptr(b2) ||
+      !ok_ptr(rw1) || !ok_ptr(rb1) || !ok_ptr(rw2) || !ok_ptr(rb2) || !ok_ptr(res_h) ||
+      !ok_ptr(res_out))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(moe_gate_topk(cfg, x, w_gate, logit_bias, buf->logits, buf->probs, buf->topk_idx,
+                        buf->topk_w, buf->slot, buf->routed_cnt, buf->kept_cnt,
+                        buf->expert_offsets, buf->row_src, buf->l_aux, workspace, workspace_bytes,
+                        stream));
+  MOE_CUDA(launch_dispatch(x, cfg->dtype, cfg->num_tokens, cfg->hidden_size, cfg->k,
+                           buf->topk_idx, buf->slot, buf->expert_offsets, buf->x_disp, stream));
+  MOE_TRY(expert_ffn(cfg, buf->x_disp, buf->expert_offsets, w1, b1, w2, b2, buf->h_pre, buf->h,
+                     buf->out_disp, stream));
+  MOE_TRY(dense_mlp(cfg, x, rw1, rb1, rw2, rb2, res_h, res_out, stream));
+  return cuda_status(launch_combine(buf->out_disp, cfg->dtype, cfg->num_tokens, cfg->hidden_size,
+                                    cfg->k, buf->topk_idx, buf->slot, buf->expert_offsets,
+                                    buf->topk_w, y, stream, res_out));
 }
 
 moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate, const void *w1,

@@ -48,13 +48,13 @@ dispatch_kernel(const uint4 *__restrict__ x, int64_t S, int nvec, int k,
   }
 }
 
-// y[s] = sum_j w[s,j] * out[row(s,j)]
+// y[s] = res[s] (if res is set) + sum_j w[s,j] * out[row(s,j)]
 template <typename T>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
                const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
                const int32_t *__restrict__ offsets, const float *__restrict__ w,
-               uint4 *__restrict__ y) {
+               const uint4 *__restrict__ res, uint4 *__restrict__ y) {
   griddep_begin();
   using V = Vec<T>;
   const int lane = threadIdx.x & 31;
@@ -66,8 +66,12 @@ combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
   const float w1 = k == 2 ? w[s * k + 1] : 0.0f;
   for (int c = lane; c < nvec; c += 32) {
     float acc[V::kN], t[V::kN];
+    if (res) {
+      V::to_f32(ld_stream(res + s * nvec + c), acc);
+    } else {
 #pragma unroll
-    for (int i = 0; i < V::kN; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < V::kN; ++i) acc[i] = 0.0f;
+    }
     if (r0 >= 0) {
       V::to_f32(ld_stream(out + r0 * nvec + c), t);
 #pragma unroll
@@ -207,16 +211,16 @@ cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
 
 cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d, int k,
                            const int32_t *idx, const int32_t *slot, const int32_t *offsets,
-                           const float *w, void *y, cudaStream_t st) {
+                           const float *w, void *y, cudaStream_t st, const void *res) {
   if (S == 0) return cudaSuccess;
   const int nvec = d * elem_bytes(dtype) / 16;
   if (dtype == MOE_F32)
     return launch_k(combine_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st,
                     static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-                    static_cast<uint4 *>(y));
+                    static_cast<const uint4 *>(res), static_cast<uint4 *>(y));
   return launch_k(combine_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st,
                   static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-                  static_cast<uint4 *>(y));
+                  static_cast<const uint4 *>(res), static_cast<uint4 *>(y));
 }
 
 cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, int64_t S,

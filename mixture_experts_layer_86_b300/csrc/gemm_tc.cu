@@ -117,7 +117,7 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *v) {
 template <bool kWMN>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-               const int32_t *__restrict__ offsets, int G, int N, int K,
+               const int32_t *__restrict__ offsets, int64_t dense_rows, int G, int N, int K,
                const __nv_bfloat16 *__restrict__ bias, int act,
                __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
@@ -146,13 +146,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
+    // without offsets the rows form one group of dense_rows rows
+    for (int g = 0; g <= G; ++g)
+      ctl.row_start[g] = offsets ? offsets[g] : (g == 0 ? 0 : int(dense_rows));
     int run = 0;
     for (int g = 0; g < G; ++g) {
       ctl.tile_start[g] = run;
-      run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
+      run += ((ctl.row_start[g + 1] - ctl.row_start[g] + kTok - 1) / kTok) * nf;
     }
     ctl.tile_start[G] = run;
-    for (int g = 0; g <= G; ++g) ctl.row_start[g] = offsets[g];
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -401,7 +403,8 @@ template <bool kWMN>
 __global__ void __launch_bounds__(kPairThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX,
-                    const int32_t *__restrict__ offsets, int G, int N, int K,
+                    const int32_t *__restrict__ offsets, int64_t dense_rows, int G, int N,
+                    int K,
                     const __nv_bfloat16 *__restrict__ bias, int act,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                     const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
@@ -432,13 +435,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
+    // without offsets the rows form one group of dense_rows rows
+    for (int g = 0; g <= G; ++g)
+      ctl.row_start[g] = offsets ? offsets[g] : (g == 0 ? 0 : int(dense_rows));
     int run = 0;
     for (int g = 0; g < G; ++g) {
       ctl.tile_start[g] = run;
-      run += ((offsets[g + 1] - offsets[g] + kTok - 1) / kTok) * nf;
+      run += ((ctl.row_start[g + 1] - ctl.row_start[g] + kTok - 1) / kTok) * nf;
     }
     ctl.tile_start[G] = run;
-    for (int g = 0; g <= G; ++g) ctl.row_start[g] = offsets[g];
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -1030,7 +1035,7 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
       pairs[dev][which] = ncl < sms / 2 ? ncl : sms / 2;
     }
     lc.gridDim = dim3(2 * pairs[dev][which]);
-    return cudaLaunchKernelEx(&lc, kern, tw, txp, g.offsets, g.G, g.N, g.K,
+    return cudaLaunchKernelEx(&lc, kern, tw, txp, g.offsets, g.rows_alloc, g.G, g.N, g.K,
                               static_cast<const __nv_bfloat16 *>(g.bias), g.act,
                               static_cast<__nv_bfloat16 *>(g.C),
                               static_cast<__nv_bfloat16 *>(g.pre),
@@ -1046,7 +1051,8 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     attr_set[which] = true;
   }
   const int grid = sms;
-  return launch_k(kern, grid, kThreads, kSmemBytes, st, tw, tx, g.offsets, g.G, g.N, g.K,
+  return launch_k(kern, grid, kThreads, kSmemBytes, st, tw, tx, g.offsets, g.rows_alloc, g.G,
+                  g.N, g.K,
                   static_cast<const __nv_bfloat16 *>(g.bias), g.act,
                   static_cast<__nv_bfloat16 *>(g.C), static_cast<__nv_bfloat16 *>(g.pre),
                   static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);

@@ -91,7 +91,7 @@ struct TcGemm {
   const void *B; bool b_kmajor;
   void *C;
   int N, K, G;
-  const int32_t *offsets;
+  const int32_t *offsets;  // [G+1] on the device; null: one group of rows_alloc rows
   const void *bias;
   int act;
   void *pre;
@@ -116,10 +116,11 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);
 cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
                             const int32_t *idx, const int32_t *slot,
                             const int32_t *offsets, void *x_disp, cudaStream_t st);
+// y[s] = res[s] (when res is not null) + sum_j w[s,j] * out_disp[row(s,j)]
 cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d,
                            int k, const int32_t *idx, const int32_t *slot,
                            const int32_t *offsets, const float *w, void *y,
-                           cudaStream_t st);
+                           cudaStream_t st, const void *res = nullptr);
 
 // ------------------------------------------------ backward helpers
 // dO[row] = w * dY[s], dw[s,j] = <dY[s], out[row]> (0 when dropped).

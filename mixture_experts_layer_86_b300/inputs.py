@@ -138,6 +138,26 @@ def skew_logit_bias(wl: Workload) -> Optional[torch.Tensor]:
                         dtype=torch.float32)
 
 
+def make_residual_weights(wl: Workload):
+    """Weights of PR-MoE's residual MLP for a workload, drawn like one
+    expert's: a CPU generator seeded with seed + 1000 draws, in float32,
+    rw1 ~ N(0, 1/d) [f, d], rw2 ~ N(0, 1/f) [d, f], then rb1 [f] and rb2 [d]
+    ~ N(0, bias_std^2) (zero when bias_std == 0), cast to the layer dtype."""
+    g = torch.Generator().manual_seed(wl.seed + 1000)
+    d, f, dt = wl.hidden_size, wl.ffn_size, wl.torch_dtype
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(dt)
+
+    rw1 = draw((f, d), 1.0 / math.sqrt(d))
+    rw2 = draw((d, f), 1.0 / math.sqrt(f))
+    if wl.bias_std > 0:
+        rb1, rb2 = draw((f,), wl.bias_std), draw((d,), wl.bias_std)
+    else:
+        rb1, rb2 = torch.zeros((f,), dtype=dt), torch.zeros((d,), dtype=dt)
+    return rw1, rb1, rw2, rb2
+
+
 def make_gate_inputs(wl: Workload):
     """x, W_g and the logit bias exactly as make_inputs draws them (the first
     two draws of the recipe), without drawing the expert weights."""

@@ -60,6 +60,28 @@ def forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, bufs=None, workspace=Non
     return y, bufs["l_aux"], bufs["kept_cnt"], bufs
 
 
+def forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
+                     bufs=None, workspace=None, y=None, stream=None):
+    """PR-MoE layer (``use_residual=True``): y = MoE(x) + MLP(x) with the
+    dense MLP weights rw1 [f,d], rb1 [f], rw2 [d,f], rb2 [d].  Returns
+    (y, l_aux, expert_count, state); state also holds the MLP's activation
+    ("res_h") and output ("res_out")."""
+    dev = x.device
+    if bufs is None:
+        bufs = alloc_buffers(cfg, dev)
+    if workspace is None:
+        workspace = alloc_workspace(cfg, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    dt = torch_dtype(cfg)
+    res_h = torch.empty((cfg.num_tokens, cfg.ffn_size), dtype=dt, device=dev)
+    res_out = torch.empty((cfg.num_tokens, cfg.hidden_size), dtype=dt, device=dev)
+    N.moe_forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, rb2, y,
+                           bufs, res_h, res_out, workspace, stream)
+    state = dict(bufs, res_h=res_h, res_out=res_out)
+    return y, bufs["l_aux"], bufs["kept_cnt"], state
+
+
 def backward(cfg, x, w_gate, w1, w2, bufs, dy, workspace=None, grads=None, stream=None):
     dev = x.device
     if workspace is None:

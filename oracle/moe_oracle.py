@@ -43,6 +43,8 @@ R5  l_aux = E * sum_e mean_s(p[s,e]) * first[e]/S, first[e] counting first
     choices before dropping.
 R6  A token whose every slot is dropped contributes y_s = 0 (no residual).
 R7  "GeLU" without qualifier is the tanh form.
+R8  PR-MoE's residual expert (use_residual=True) is combined with the MoE
+    output by a sum, y = MoE(x) + MLP(x); the page gives no mixing formula.
 
 Parity pins (tests/test_oracle_pins.py): brute-force top-k and slot
 enumeration on tiny inputs, hand-worked capacity/drop cases, the pages' own
@@ -366,6 +368,29 @@ def dense_mixture(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, logit_bias=None):
         ye = he @ np.asarray(w2[e], np.float64).T + np.asarray(b2[e], np.float64)
         y += mix[:, e:e + 1] * ye
     return y
+
+
+def residual_mlp(x, rw1, rb1, rw2, rb2, act: str) -> np.ndarray:
+    """PR-MoE's fixed MLP on every token ([deepspeed.moe overview] §2.3 and
+    §3.3: ``use_residual=True`` combines a fixed MLP with the dynamic
+    experts): act(x rw1^T + rb1) rw2^T + rb2, the shape of one expert."""
+    x = np.asarray(x, np.float64)
+    h = activation(x @ np.asarray(rw1, np.float64).T + np.asarray(rb1, np.float64), act)
+    return h @ np.asarray(rw2, np.float64).T + np.asarray(rb2, np.float64)
+
+
+def forward_residual(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
+                     logit_bias=None, logits: Optional[np.ndarray] = None) -> dict:
+    """The PR-MoE layer.  The page names the residual connection but gives no
+    mixing formula; reading R8: the connection is a sum,
+    y = MoE(x) + MLP(x).  Returns ``forward``'s dict with ``y`` replaced and
+    ``y_moe`` / ``residual`` added."""
+    g = forward(cfg, x, w_gate, w1, b1, w2, b2, logit_bias=logit_bias, logits=logits)
+    r = residual_mlp(x, rw1, rb1, rw2, rb2, cfg.act)
+    g["y_moe"] = g["y"]
+    g["residual"] = r
+    g["y"] = g["y_moe"] + r
+    return g
 
 
 # ---------------------------------------------------------------------------

@@ -289,6 +289,40 @@ def test_single_expert_is_plain_ffn():
     assert np.allclose(y, ref, rtol=1e-13, atol=1e-13)
 
 
+@pytest.mark.parametrize("act,tact", [(O.ACT_RELU, "relu"), (O.ACT_GELU_TANH, "tanh")])
+def test_residual_layer_adds_a_dense_mlp(act, tact):
+    """PR-MoE (reading R8): y_res - y_moe is torch's Linear -> act -> Linear
+    on every token; zero residual weights give the plain layer exactly; with
+    one expert, k=1 and the expert's weights as the residual's, y = 2 FFN(x)."""
+    rng = np.random.default_rng(21)
+    S, d, f, E = 30, 6, 9, 4
+    c = cfg(S, d, f, E, 2, cf=0.75, min_cap=1, act=act)
+    x = rng.standard_normal((S, d))
+    wg = rng.standard_normal((E, d))
+    w1, b1 = rng.standard_normal((E, f, d)), rng.standard_normal((E, f))
+    w2, b2 = rng.standard_normal((E, d, f)), rng.standard_normal((E, d))
+    rw1, rb1 = rng.standard_normal((f, d)), rng.standard_normal(f)
+    rw2, rb2 = rng.standard_normal((d, f)), rng.standard_normal(d)
+    g = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, rw2, rb2)
+    F = torch.nn.functional
+    z = F.linear(torch.from_numpy(x), torch.from_numpy(rw1), torch.from_numpy(rb1))
+    hz = F.relu(z) if tact == "relu" else F.gelu(z, approximate=tact)
+    mlp = F.linear(hz, torch.from_numpy(rw2), torch.from_numpy(rb2)).numpy()
+    assert np.allclose(g["y"] - g["y_moe"], mlp, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(g["y_moe"], O.forward(c, x, wg, w1, b1, w2, b2)["y"])
+    zero = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, np.zeros((d, f)), np.zeros(d))
+    assert np.array_equal(zero["y"], zero["y_moe"])
+    c1 = cfg(S, d, f, 1, 1, cf=1.0, min_cap=1, act=act)
+    one = O.forward_residual(c1, x, wg[:1], w1[:1], b1[:1], w2[:1], b2[:1],
+                             w1[0], b1[0], w2[0], b2[0])
+    ffn = F.linear(F.relu(F.linear(torch.from_numpy(x), torch.from_numpy(w1[0]),
+                                   torch.from_numpy(b1[0]))) if tact == "relu" else
+                   F.gelu(F.linear(torch.from_numpy(x), torch.from_numpy(w1[0]),
+                                   torch.from_numpy(b1[0])), approximate=tact),
+                   torch.from_numpy(w2[0]), torch.from_numpy(b2[0])).numpy()
+    assert np.allclose(one["y"], 2.0 * ffn, rtol=1e-12, atol=1e-12)
+
+
 @pytest.mark.parametrize("k", [1, 2])
 def test_no_drop_equals_dense_mixture(k):
     rng = np.random.default_rng(10 + k)
