@@ -65,10 +65,26 @@ typedef enum {
   MOE_ACT_GELU_ERF = 2   /* 0.5 z (1 + erf(z / sqrt 2))                      */
 } moe_act;
 
+typedef enum {
+  MOE_AUX_LOAD = 0, /* l_aux = E * sum_e mean_s(p[s,e]) * first[e] / S           */
+  MOE_AUX_STD = 1   /* l_aux = std_e(mean_s p[s,e]) + 1e-6 (population std)    */
+} moe_aux_loss;
+
 /* Mirrors MoE(hidden_size, num_experts, k, capacity_factor, min_capacity,
  * drop_tokens) of the deepspeed.moe overview, §2.1, plus the expert FFN
  * width, activation, element type and the weight of l_aux in the training
- * loss L = <dY, y> + aux_loss_weight * l_aux. */
+ * loss L = <dY, y> + aux_loss_weight * l_aux, and three gating variants:
+ *  - gate_temperature T (the gating_softmax_temp of the DeepSpeed config on
+ *    the ZeRO-3 + MoE page): p = softmax(logits / T); T = 0 means 1.  The
+ *    top-k choice is unchanged for any T > 0.
+ *  - aux_loss_type: the balance loss of the layer's specification, or the
+ *    DeepSeek-MoE page's std-based alternative lambda * (std(usage) + 1e-6)
+ *    with usage[e] = mean over tokens of p[s,e] (ch.1 load-balancing table).
+ *  - logit_bias_per_token: logit_bias is [S,E] instead of [E].  Noisy gating
+ *    (noisy_gate_policy, deepspeed.moe overview §2.1 / §3.1) adds random
+ *    noise to the gate logits; the caller draws that noise and passes it
+ *    here, so the layer itself stays deterministic.  A per-token bias gets
+ *    no gradient. */
 typedef struct {
   int64_t num_tokens;      /* S >= 0                                        */
   int32_t hidden_size;     /* d                                             */
@@ -81,6 +97,9 @@ typedef struct {
   int32_t act;             /* moe_act                                        */
   int32_t dtype;           /* moe_dtype                                      */
   float aux_loss_weight;   /* backward only                                  */
+  float gate_temperature;  /* >= 0; 0 or 1 = plain softmax                   */
+  int32_t aux_loss_type;   /* moe_aux_loss                                   */
+  int32_t logit_bias_per_token; /* nonzero: logit_bias is [S,E], else [E]    */
 } moe_config;
 
 /* Saved state of one forward pass (all device pointers, caller-owned).

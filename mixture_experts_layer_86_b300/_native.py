@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_b300
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_RELU, MOE_ACT_GELU_TANH, MOE_ACT_GELU_ERF = 0, 1, 2
+MOE_AUX_LOAD, MOE_AUX_STD = 0, 1
+AUX_CODES = {"load": MOE_AUX_LOAD, "std": MOE_AUX_STD}
 ACT_CODES = {"relu": MOE_ACT_RELU, "gelu_tanh": MOE_ACT_GELU_TANH, "gelu_erf": MOE_ACT_GELU_ERF}
 DTYPE_CODES = {"f32": MOE_F32, "bf16": MOE_BF16}
 
@@ -26,7 +28,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("num_tokens", c_int64), ("hidden_size", c_int32), ("ffn_size", c_int32),
                 ("num_experts", c_int32), ("k", c_int32), ("capacity_factor", c_double),
                 ("min_capacity", c_int32), ("drop_tokens", c_int32), ("act", c_int32),
-                ("dtype", c_int32), ("aux_loss_weight", c_float)]
+                ("dtype", c_int32), ("aux_loss_weight", c_float), ("gate_temperature", c_float),
+                ("aux_loss_type", c_int32), ("logit_bias_per_token", c_int32)]
 
 
 class MoeBuffers(ctypes.Structure):
@@ -109,18 +112,23 @@ def _stream(stream):
 
 def make_config(num_tokens, hidden_size, ffn_size, num_experts, k, capacity_factor,
                 min_capacity, drop_tokens, act="gelu_tanh", dtype="bf16",
-                aux_loss_weight=0.0) -> MoeConfig:
+                aux_loss_weight=0.0, gate_temperature=1.0, aux_loss_type="load",
+                logit_bias_per_token=False) -> MoeConfig:
     return MoeConfig(int(num_tokens), int(hidden_size), int(ffn_size), int(num_experts), int(k),
                      float(capacity_factor), int(min_capacity), int(bool(drop_tokens)),
                      ACT_CODES[act] if isinstance(act, str) else int(act),
                      DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype),
-                     float(aux_loss_weight))
+                     float(aux_loss_weight), float(gate_temperature),
+                     AUX_CODES[aux_loss_type] if isinstance(aux_loss_type, str)
+                     else int(aux_loss_type), int(bool(logit_bias_per_token)))
 
 
 def config_from_workload(wl, num_tokens=None) -> MoeConfig:
     return make_config(wl.num_tokens if num_tokens is None else num_tokens, wl.hidden_size,
                        wl.ffn_size, wl.num_experts, wl.k, wl.capacity_factor, wl.min_capacity,
-                       wl.drop_tokens, wl.act, wl.dtype, wl.aux_loss_weight)
+                       wl.drop_tokens, wl.act, wl.dtype, wl.aux_loss_weight,
+                       getattr(wl, "gate_temperature", 1.0), getattr(wl, "aux_loss_type", "load"),
+                       getattr(wl, "logit_noise_std", 0.0) > 0)
 
 
 # ---------------------------------------------------------------- host-only

@@ -19,6 +19,10 @@ constexpr int kMaxDevices = 64;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+float inv_temperature(const moe_config *c) {
+  return c->gate_temperature > 0.0f ? 1.0f / c->gate_temperature : 1.0f;
+}
+
 unsigned int *device_error_ptr() {
   static unsigned int *ptrs[kMaxDevices] = {nullptr};
   static std::mutex mu;
@@ -46,6 +50,10 @@ moe_status check_config(const moe_config *c) {
   if (c->min_capacity < 0) return MOE_ERR_INVALID_ARG;
   if (c->act < MOE_ACT_RELU || c->act > MOE_ACT_GELU_ERF) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!(c->gate_temperature >= 0.0f) || c->gate_temperature > 1e30f) return MOE_ERR_INVALID_ARG;
+  if (c->aux_loss_type != MOE_AUX_LOAD && c->aux_loss_type != MOE_AUX_STD)
+    return MOE_ERR_INVALID_ARG;
+  if (c->logit_bias_per_token != 0 && c->logit_bias_per_token != 1) return MOE_ERR_INVALID_ARG;
   if (c->num_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (c->num_tokens * c->k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -77,7 +85,7 @@ size_t fwd_ws_bytes(const moe_config *c) {
 struct BwdWs {
   void *d_out, *dh_pre, *dx_disp;
   float *dw, *dlogits, *gate_partial;
-  int32_t *first;
+  float *aux_coef;
 };
 
 size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
@@ -99,7 +107,7 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->dw = reinterpret_cast<float *>(p); p += sz[3];
     w->dlogits = reinterpret_cast<float *>(p); p += sz[4];
     w->gate_partial = reinterpret_cast<float *>(p); p += sz[5];
-    w->first = reinterpret_cast<int32_t *>(p);
+    w->aux_coef = reinterpret_cast<float *>(p);
   }
   size_t total = 0;
   for (size_t v : sz) total += v;
@@ -127,6 +135,7 @@ moe_status gate_gemm(const moe_config *c, const void *x, const void *w_gate,
   g.M = c->num_tokens; g.N = c->num_experts; g.K = c->hidden_size;
   g.mode = 0;
   g.bias_f32 = logit_bias;
+  g.bias_f32_ld = c->logit_bias_per_token ? c->num_experts : 0;
   g.act = -1;
   return cuda_status(launch_simt_gemm(g, st));
 }
@@ -137,6 +146,8 @@ moe_status route(const moe_config *c, const float *logits, float *probs, int32_t
   RouteArgs a{};
   a.logits = logits; a.S = c->num_tokens; a.E = c->num_experts; a.k = c->k;
   a.cap = capacity_of(c);
+  a.inv_temp = inv_temperature(c);
+  a.aux_type = c->aux_loss_type;
   a.probs = probs; a.idx = idx; a.w = w; a.slot = slot;
   a.routed = routed; a.kept = kept; a.offsets = offsets; a.row_src = row_src; a.l_aux = l_aux;
   route_carve_workspace(a, ws);
@@ -295,12 +306,16 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x, const void *w_gat
     // fused tensor-core gate, then the shared scan / assignment
     RouteArgs a{};
     a.S = cfg->num_tokens; a.E = cfg->num_experts; a.k = cfg->k; a.cap = capacity_of(cfg);
+    a.inv_temp = inv_temperature(cfg);
+    a.aux_type = cfg->aux_loss_type;
     a.probs = probs; a.idx = topk_idx; a.w = topk_w; a.slot = slot; a.routed = routed_cnt;
     a.kept = kept_cnt; a.offsets = expert_offsets; a.row_src = row_src; a.l_aux = l_aux;
     route_carve_workspace(a, workspace);
     GateTcArgs g{};
     g.x = x; g.w_gate = w_gate; g.S = cfg->num_tokens; g.d = cfg->hidden_size;
     g.E = cfg->num_experts; g.k = cfg->k; g.logit_bias = logit_bias; g.logits = logits;
+    g.bias_ld = cfg->logit_bias_per_token ? cfg->num_experts : 0;
+    g.inv_temp = inv_temperature(cfg);
     g.probs = probs; g.idx = topk_idx; g.w = topk_w; g.rank = slot; g.hist = a.hist;
     g.psum = a.psum; g.err = device_error_ptr();
     MOE_CUDA(launch_gate_tc(g, stream));
@@ -489,9 +504,10 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     }
   }
   // 6. router: dlogits, dW_g = dlogits^T x
-  MOE_CUDA(launch_first_count(sv->topk_idx, S, k, E, w.first, st));
-  MOE_CUDA(launch_gate_bwd(sv->probs, sv->topk_idx, w.dw, w.first, S, E, k,
-                           cfg->aux_loss_weight, w.dlogits, st));
+  MOE_CUDA(launch_aux_coef(sv->topk_idx, sv->probs, S, k, E, cfg->aux_loss_type, w.aux_coef,
+                           st));
+  MOE_CUDA(launch_gate_bwd(sv->probs, sv->topk_idx, w.dw, w.aux_coef, S, E, k,
+                           cfg->aux_loss_weight, inv_temperature(cfg), w.dlogits, st));
   MOE_CUDA(launch_gate_wgrad(w.dlogits, x, dt, S, d, E, w.gate_partial, dw_gate, st));
   // 7. dX = sum_j dx_disp[row] + dlogits W_g
   return cuda_status(launch_dx_combine(w.dx_disp, w.dlogits, w_gate, dt, S, d, E, k,

@@ -144,22 +144,72 @@ __global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N
   }
 }
 
-__global__ void first_count_kernel(const int32_t *__restrict__ idx, int64_t S, int k,
-                                   int E, int32_t *__restrict__ first) {
+// d l_aux / d p[s,e], the same for every token (one CTA):
+//   MOE_AUX_LOAD: E * first[e] / S^2   (first[e] = tokens whose first choice is e)
+//   MOE_AUX_STD:  (u_e - mean u) / (E * S * std u),  u_e = mean_s p[s,e],
+//                 population std; 0 when std u = 0
+__global__ void aux_coef_kernel(const int32_t *__restrict__ idx, const float *__restrict__ probs,
+                                int64_t S, int k, int E, int aux_type, float *__restrict__ coef) {
   griddep_begin();
+  __shared__ double s_col[kMaxExperts];
+  __shared__ double s_part[1024];
   __shared__ int32_t cnt[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __shared__ double s_stat[2];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    s_col[e] = 0.0;
+  }
   __syncthreads();
-  for (int64_t s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&cnt[idx[s * k]], 1);
+  if (aux_type == MOE_AUX_STD) {
+    // column sums of p: G token groups per column (consecutive threads on
+    // consecutive columns), then the groups added in a fixed order
+    const int G = int(blockDim.x) / E;
+    const int e = threadIdx.x % E, grp = threadIdx.x / E;
+    if (grp < G) {
+      double acc = 0.0;
+      for (int64_t s = grp; s < S; s += G) acc += double(probs[s * E + e]);
+      s_part[grp * E + e] = acc;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < E; c += blockDim.x) {
+      double acc = 0.0;
+      for (int g = 0; g < G; ++g) acc += s_part[g * E + c];
+      s_col[c] = acc;
+    }
+  } else {
+    for (int64_t s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&cnt[idx[s * k]], 1);
+  }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) first[e] = cnt[e];
+  if (threadIdx.x == 0 && aux_type == MOE_AUX_STD) {
+    double su = 0.0, sq = 0.0;
+    for (int e = 0; e < E; ++e) su += s_col[e] / double(S);
+    const double mean = su / double(E);
+    for (int e = 0; e < E; ++e) {
+      const double dv = s_col[e] / double(S) - mean;
+      sq += dv * dv;
+    }
+    s_stat[0] = mean;
+    s_stat[1] = sqrt(sq / double(E));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    double c;
+    if (aux_type == MOE_AUX_STD)
+      c = s_stat[1] > 0.0 ? (s_col[e] / double(S) - s_stat[0]) /
+                                (double(E) * double(S) * s_stat[1])
+                          : 0.0;
+    else
+      c = double(E) * double(cnt[e]) / (double(S) * double(S));
+    coef[e] = float(c);
+  }
 }
 
 // One warp per token; lanes over experts.
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx,
-                const float *__restrict__ dw, const int32_t *__restrict__ first,
-                int64_t S, int E, int k, float aux_scale, float *__restrict__ dlogits) {
+                const float *__restrict__ dw, const float *__restrict__ coef,
+                int64_t S, int E, int k, float aux_w, float inv_temp,
+                float *__restrict__ dlogits) {
   griddep_begin();
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
@@ -181,17 +231,17 @@ gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx
   }
   float dot = 0.0f;
   for (int e = lane; e < E; e += 32) {
-    float dp = aux_scale * float(first[e]);
+    float dp = aux_w * coef[e];
     if (e == i1) dp += g1;
     if (e == i2) dp += g2;
     dot = fmaf(dp, p[e], dot);
   }
   dot = warp_sum(dot);
   for (int e = lane; e < E; e += 32) {
-    float dp = aux_scale * float(first[e]);
+    float dp = aux_w * coef[e];
     if (e == i1) dp += g1;
     if (e == i2) dp += g2;
-    dlogits[s * E + e] = p[e] * (dp - dot);
+    dlogits[s * E + e] = inv_temp * p[e] * (dp - dot);  // the softmax saw logits / T
   }
 }
 
@@ -245,19 +295,18 @@ cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
   return launch_k(group_colsum_kernel, grid, dim3(32, 8), 0, st, M, dtype, N, offsets, db);
 }
 
-cudaError_t launch_first_count(const int32_t *idx, int64_t S, int k, int E, int32_t *first,
-                               cudaStream_t st) {
-  return launch_k(first_count_kernel, 1, 1024, 0, st, idx, S, k, E, first);
+cudaError_t launch_aux_coef(const int32_t *idx, const float *probs, int64_t S, int k, int E,
+                            int aux_type, float *coef, cudaStream_t st) {
+  if (S == 0) return cudaMemsetAsync(coef, 0, sizeof(float) * E, st);
+  return launch_k(aux_coef_kernel, 1, 1024, 0, st, idx, probs, S, k, E, aux_type, coef);
 }
 
 cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float *dw,
-                            const int32_t *first, int64_t S, int E, int k, float aux_w,
-                            float *dlogits, cudaStream_t st) {
+                            const float *coef, int64_t S, int E, int k, float aux_w,
+                            float inv_temp, float *dlogits, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
-  // d(aux_w * l_aux)/dp[s,e] = aux_w * E * first[e] / S^2
-  const float aux_scale = float(double(aux_w) * double(E) / (double(S) * double(S)));
-  return launch_k(gate_bwd_kernel, token_blocks(S), kWarpsPerCta * 32, 0, st, probs, idx, dw, first,
-                  S, E, k, aux_scale, dlogits);
+  return launch_k(gate_bwd_kernel, token_blocks(S), kWarpsPerCta * 32, 0, st, probs, idx, dw,
+                  coef, S, E, k, aux_w, inv_temp, dlogits);
 }
 
 }  // namespace moe

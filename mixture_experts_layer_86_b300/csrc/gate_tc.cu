@@ -10,10 +10,12 @@
 // follows is latency-bound, so it is spread over all 16 warps of the CTA:
 //   warp 0      TMA producer (x tile 128 x 64, W_g tile E x 64 per stage)
 //   warp 1      TMEM allocator + MMA issuer
-//   warps 4..7  copy the 128 x E fp32 logits (+ bias) from TMEM into a
+//   warps 4..7  copy the 128 x E fp32 logits (+ the per-expert or
+//               per-token logit bias) from TMEM into a
 //               shared-memory tile (the ring buffers are idle by then)
 //   all warps   4 lanes per token, each over a quarter of the experts:
-//               top-2 with ties to the lower index, softmax, weights;
+//               top-2 with ties to the lower index, softmax of logits / T
+//               (the gate temperature), weights;
 //               coalesced row copies of logits / probabilities; per-expert
 //               probability sums over the CTA's tokens
 //   warps 4..7  the CTA's count and rank of every (choice, expert) pair in
@@ -78,7 +80,8 @@ __device__ __forceinline__ void epi_sync() {
 __global__ void __launch_bounds__(kGateThreads, 1)
 gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                int64_t S, int d, int E, int E_pad, int k, uint32_t idesc, uint32_t tmem_cols,
-               int nstages, uint32_t ring_bytes, const float *__restrict__ logit_bias, float *__restrict__ logits_out,
+               int nstages, uint32_t ring_bytes, const float *__restrict__ logit_bias,
+               int bias_ld, float inv_temp, float *__restrict__ logits_out,
                float *__restrict__ probs_out, int32_t *__restrict__ idx_out,
                float *__restrict__ w_out, int32_t *__restrict__ rank_out,
                int32_t *__restrict__ hist, float *__restrict__ psum_out, int64_t nblk,
@@ -183,6 +186,11 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     ptx::tc_fence_after();
     const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
     float *row = tile + r * ldt;
+    // the logit bias of this token: one row for all tokens, or its own row
+    const float *bias_row =
+        logit_bias == nullptr || (bias_ld != 0 && tok0 + r >= S)
+            ? nullptr
+            : logit_bias + (bias_ld != 0 ? (tok0 + r) * bias_ld : 0);
     for (int c = 0; c < (E + 31) / 32; ++c) {
       uint32_t raw[32];
       ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
@@ -190,7 +198,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         const int e = c * 32 + t;
-        if (e < E) row[e] = __uint_as_float(raw[t]) + (logit_bias ? logit_bias[e] : 0.0f);
+        if (e < E) row[e] = __uint_as_float(raw[t]) + (bias_row ? bias_row[e] : 0.0f);
       }
     }
     ptx::tc_fence_before();
@@ -225,10 +233,10 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   float za = 0.0f, zb = 0.0f;
   int ez = c0;
   for (; ez + 1 < c1; ez += 2) {
-    za += expf(trow_s[ez] - m);
-    zb += expf(trow_s[ez + 1] - m);
+    za += expf((trow_s[ez] - m) * inv_temp);
+    zb += expf((trow_s[ez + 1] - m) * inv_temp);
   }
-  if (ez < c1) za += expf(trow_s[ez] - m);
+  if (ez < c1) za += expf((trow_s[ez] - m) * inv_temp);
   float z = za + zb;
   z += __shfl_xor_sync(kFullMask, z, 1);
   z += __shfl_xor_sync(kFullMask, z, 2);
@@ -236,7 +244,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   block_sync();  // every read of the logits tile is done
 
   // probabilities replace the logits in the tile (0 for tokens >= S)
-  for (int e = c0; e < c1; ++e) trow_s[e] = valid ? expf(trow_s[e] - m) * inv_z : 0.0f;
+  for (int e = c0; e < c1; ++e) trow_s[e] = valid ? expf((trow_s[e] - m) * inv_temp) * inv_z : 0.0f;
   if (seg == 0) {
     const int i1 = best1.i, i2 = best2.i;
     if (valid) {
@@ -244,7 +252,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       if (k == 1) {
         w_out[s] = inv_z;  // exp(l1 - max) = 1
       } else {
-        const float x2 = expf(best2.v - m);
+        const float x2 = expf((best2.v - m) * inv_temp);
         const float den = 1.0f + x2;
         w_out[s * 2] = 1.0f / den;
         w_out[s * 2 + 1] = x2 / den;
@@ -378,7 +386,8 @@ cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st) {
   }
   const uint32_t idesc = ptx::idesc_bf16(GBM, E_pad, 0, 0);
   return launch_k(gate_tc_kernel, unsigned(nblk), kGateThreads, smem, st, tx, tw, a.S, a.d, a.E,
-                  E_pad, a.k, idesc, cols, nstages, uint32_t(ring), a.logit_bias, a.logits, a.probs,
+                  E_pad, a.k, idesc, cols, nstages, uint32_t(ring), a.logit_bias, a.bias_ld,
+                  a.inv_temp, a.logits, a.probs,
                   a.idx, a.w, a.rank, a.hist, a.psum, nblk, a.err);
 }
 

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(SimtGemm g) {
       if (n >= g.N) continue;
       float v = acc[i][j];
       if (g.bias) v += load_elem(g.bias, g.b_dtype, int64_t(grp) * g.bias_g + n);
-      if (g.bias_f32) v += g.bias_f32[n];
+      if (g.bias_f32) v += g.bias_f32[(row0 + mm) * g.bias_f32_ld + n];
       const int64_t ci = c_base + (row0 + mm) * g.c_m + int64_t(n) * g.c_n;
       if (g.pre) store_elem(g.pre, g.c_dtype, ci, v);
       if (g.act >= 0) v = act_fwd(v, g.act);

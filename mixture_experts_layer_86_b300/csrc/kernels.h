@@ -13,10 +13,12 @@ constexpr int kRouteTokensPerCta = 128;
 
 // ---------------------------------------------------------------- routing
 struct RouteArgs {
-  const float *logits;  // [S,E] fp32
+  const float *logits;  // [S,E] fp32 (bias included)
   int64_t S;
   int E, k;
   int64_t cap;          // -1: no capacity limit
+  float inv_temp;       // 1 / gate temperature: p = softmax(logits * inv_temp)
+  int aux_type;         // MOE_AUX_LOAD or MOE_AUX_STD
   float *probs;         // [S,E] or null
   int32_t *idx;         // [S,k]
   float *w;             // [S,k]
@@ -41,7 +43,9 @@ struct GateTcArgs {
   const void *x, *w_gate;   // bf16 [S,d], [E,d]
   int64_t S;
   int d, E, k;
-  const float *logit_bias;  // [E] or null
+  const float *logit_bias;  // [E] (bias_ld 0) or [S,E] (bias_ld E), or null
+  int bias_ld;
+  float inv_temp;           // 1 / gate temperature
   float *logits, *probs;    // [S,E] or null
   int32_t *idx;
   float *w;
@@ -72,7 +76,8 @@ struct SimtGemm {
   const int32_t *offsets; int G;
   int64_t max_rows;
   const void *bias; int64_t bias_g;     // element type b_dtype
-  const float *bias_f32;                // fp32 bias over n (mode 0)
+  const float *bias_f32;                // fp32 bias over n (mode 0): bias_f32[m*ld + n]
+  int64_t bias_f32_ld;                  // 0: one row for all m
   int act;                              // -1 none
   void *pre;                            // same layout/type as C
   const void *grad_src; int dact;       // same layout/type as C
@@ -133,14 +138,17 @@ cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype,
 cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
                                 const int32_t *offsets, void *db,
                                 cudaStream_t st);
-// first[e] = number of tokens whose first choice is e.
-cudaError_t launch_first_count(const int32_t *idx, int64_t S, int k, int E,
-                               int32_t *first, cudaStream_t st);
-// dlogits = p * (dp - <dp,p>), dp from dw through the weights and the
-// l_aux term aux_w * E * first[e] / S^2.
+// coef[e] = d l_aux / d p[s,e] (the same for every token): E*first[e]/S^2
+// for MOE_AUX_LOAD, (u_e - mean u) / (E * S * std u) with u_e = mean_s
+// p[s,e] for MOE_AUX_STD (0 when std u = 0).
+cudaError_t launch_aux_coef(const int32_t *idx, const float *probs, int64_t S, int k, int E,
+                            int aux_type, float *coef, cudaStream_t st);
+// dlogits = inv_temp * p * (dp - <dp,p>), dp from dw through the weights
+// and the l_aux term aux_w * coef[e]: the gradient of the logits the gate
+// GEMM produced (before the 1/T scaling).
 cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx,
-                            const float *dw, const int32_t *first, int64_t S,
-                            int E, int k, float aux_w, float *dlogits,
+                            const float *dw, const float *coef, int64_t S,
+                            int E, int k, float aux_w, float inv_temp, float *dlogits,
                             cudaStream_t st);
 // dW_g = dlogits^T x: token-split fp32 partial sums, then a fixed-order sum.
 int64_t gate_wgrad_splits(int64_t S);

@@ -34,7 +34,7 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __global__ void __launch_bounds__(kTB)
-route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
+route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, float inv_temp,
                   float *__restrict__ probs, int32_t *__restrict__ idx_out,
                   float *__restrict__ w_out, int32_t *__restrict__ rank_out,
                   int32_t *__restrict__ hist, float *__restrict__ psum) {
@@ -76,7 +76,7 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k,
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
       const int e = lane + 32 * q;
-      ex[q] = (q < nq && e < E) ? expf(v[q] - m) : 0.0f;
+      ex[q] = (q < nq && e < E) ? expf((v[q] - m) * inv_temp) : 0.0f;
       z += ex[q];
     }
     z = warp_sum(z);
@@ -192,7 +192,7 @@ constexpr int kScanMaxGroups = 32;
 // B300's slow float64 pipe (a partial is at most the CTA's token count, so
 // S < 2^31 keeps every total below 2^61).
 __global__ void __launch_bounds__(kScanThreads)
-route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
+route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_type,
                   int32_t *__restrict__ hist, const float *__restrict__ psum,
                   int32_t *__restrict__ first_cnt, int32_t *__restrict__ routed,
                   int32_t *__restrict__ kept, int32_t *__restrict__ offsets,
@@ -285,8 +285,24 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap,
     if (lane == 31) offsets[E] = incl;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
-    // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
-    if (lane == 0) *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
+    if (aux_type == MOE_AUX_STD) {
+      // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
+      double su = 0.0, sq = 0.0;
+      for (int e = e0; e < e1; ++e) su += S > 0 ? s_aux[e] / double(S) : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(kFullMask, su, o);
+      const double mean = su / double(E);
+      for (int e = e0; e < e1; ++e) {
+        const double dv = (S > 0 ? s_aux[e] / double(S) : 0.0) - mean;
+        sq += dv * dv;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
+      if (lane == 0) *l_aux = float(sqrt(sq / double(E)) + 1e-6);
+    } else {
+      // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
+      if (lane == 0) *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
+    }
   }
 }
 
@@ -334,8 +350,8 @@ void route_carve_workspace(RouteArgs &a, void *ws) {
 cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st) {
   const int64_t nblk = (a.S + kTB - 1) / kTB;
   if (const cudaError_t e = launch_k(route_scan_kernel, 1, kScanThreads, 0, st, nblk, a.S, a.E, a.k,
-                                     a.cap, a.hist, a.psum, a.first_cnt, a.routed, a.kept, a.offsets,
-                                     a.l_aux); e != cudaSuccess)
+                                     a.cap, a.aux_type, a.hist, a.psum, a.first_cnt, a.routed,
+                                     a.kept, a.offsets, a.l_aux); e != cudaSuccess)
     return e;
   const int64_t n = a.S * a.k;
   if (n > 0) {
@@ -351,8 +367,8 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   const int64_t nblk = (a.S + kTB - 1) / kTB;
   if (nblk > 0) {
     if (const cudaError_t e = launch_k(route_topk_kernel, unsigned(nblk), kTB, 0, st, a.logits, a.S,
-                                       a.E, a.k, a.probs, a.idx, a.w, a.slot, a.hist,
-                                       a.psum); e != cudaSuccess)
+                                       a.E, a.k, a.inv_temp, a.probs, a.idx, a.w, a.slot,
+                                       a.hist, a.psum); e != cudaSuccess)
       return e;
   }
   const cudaError_t e = cudaGetLastError();

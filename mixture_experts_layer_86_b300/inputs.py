@@ -15,7 +15,9 @@ seed draws, in this order and in float32,
   dY ~ N(0,1)                   [S, d]        (only when a backward is run)
 and casts each to the workload dtype with round-to-nearest-even.  The
 skewed-routing workload adds a constant per-expert logit bias
-b_e = skew * ln(1/(e+1)) (fp32), i.e. expert e has Zipf rank e.
+b_e = skew * ln(1/(e+1)) (fp32), i.e. expert e has Zipf rank e.  A workload
+with gate noise finally draws a per-token logit noise [S, E] ~
+N(0, logit_noise_std^2) (fp32); the logit bias is then [S, E].
 """
 from __future__ import annotations
 
@@ -44,6 +46,9 @@ class Workload:
     bias_std: float = 0.0
     aux_loss_weight: float = 0.0
     backward: bool = False
+    gate_temperature: float = 1.0   # softmax temperature of the gate
+    aux_loss_type: str = "load"     # "load" | "std"
+    logit_noise_std: float = 0.0    # > 0: per-token gate noise N(0, std^2), [S, E]
 
     def scaled(self, num_tokens: int, **kw) -> "Workload":
         """Same layer shape and routing settings with a different batch."""
@@ -126,7 +131,13 @@ def make_inputs(wl: Workload, with_dy: Optional[bool] = None,
     dy = None
     if wl.backward if with_dy is None else with_dy:
         dy = draw((S, d), 1.0)
-    return LayerInputs(x, w_gate, w1, b1, w2, b2, skew_logit_bias(wl), dy)
+    logit_bias = skew_logit_bias(wl)
+    if wl.logit_noise_std > 0:
+        # noisy gating: the caller's per-token logit noise, drawn last so the
+        # other tensors do not depend on it
+        noise = torch.randn((S, E), generator=g, dtype=torch.float32) * wl.logit_noise_std
+        logit_bias = noise if logit_bias is None else noise + logit_bias[None, :]
+    return LayerInputs(x, w_gate, w1, b1, w2, b2, logit_bias, dy)
 
 
 def skew_logit_bias(wl: Workload) -> Optional[torch.Tensor]:

@@ -45,6 +45,13 @@ R6  A token whose every slot is dropped contributes y_s = 0 (no residual).
 R7  "GeLU" without qualifier is the tanh form.
 R8  PR-MoE's residual expert (use_residual=True) is combined with the MoE
     output by a sum, y = MoE(x) + MLP(x); the page gives no mixing formula.
+R9  The std-based balance loss lambda * (std(usage_prob) + 1e-6) reads
+    usage_prob[e] as mean_s p[s,e] (the differentiable usage), with the
+    population std over experts.
+R10 The gate temperature T (gating_softmax_temp) divides the logits before
+    the softmax; the top-k choice (taken on the logits) is unchanged.
+    Noisy gating adds caller-drawn noise to the logits as a per-token bias
+    [S,E] (the layer itself stays deterministic; the noise gets no gradient).
 
 Parity pins (tests/test_oracle_pins.py): brute-force top-k and slot
 enumeration on tiny inputs, hand-worked capacity/drop cases, the pages' own
@@ -99,7 +106,8 @@ def gate_logits(x: np.ndarray, w_gate: np.ndarray,
     """
     lg = np.asarray(x, np.float64) @ np.asarray(w_gate, np.float64).T
     if logit_bias is not None:
-        lg = lg + np.asarray(logit_bias, np.float64)[None, :]
+        b = np.asarray(logit_bias, np.float64)
+        lg = lg + (b[None, :] if b.ndim == 1 else b)   # [E] or per-token [S,E]
     return lg
 
 
@@ -143,14 +151,21 @@ def gate_weights(probs: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return p_sel / p_sel.sum(axis=1, keepdims=True)
 
 
-def aux_loss(probs: np.ndarray, idx: np.ndarray) -> float:
-    """Load-balancing loss l_aux = E * sum_e mean_s(p[s,e]) * first[e]/S.
+def aux_loss(probs: np.ndarray, idx: np.ndarray, kind: str = "load") -> float:
+    """Load-balancing loss.
 
-    The pages name the term (``gate_loss``, weight 0.01) without a formula;
-    this is the definition the layer is specified with (reading R5).
+    ``load``: l_aux = E * sum_e mean_s(p[s,e]) * first[e]/S.  The pages name
+    the term (``gate_loss``, weight 0.01) without a formula; this is the
+    definition the layer is specified with (reading R5).
+    ``std``: the DeepSeek-MoE page's alternative, lambda * (std(usage_prob)
+    + 1e-6) ([DeepSeek-MoE traps] ch.1 load-balancing table); reading R9:
+    usage_prob[e] = mean_s p[s,e], std over experts (population).
     """
     p = np.asarray(probs, np.float64)
     S, E = p.shape
+    if kind == "std":
+        u = p.mean(axis=0)
+        return float(np.sqrt(np.mean((u - u.mean()) ** 2)) + 1e-6)
     first = np.bincount(idx[:, 0], minlength=E).astype(np.float64)
     return float(E * np.sum(p.mean(axis=0) * (first / S)))
 
@@ -312,19 +327,21 @@ class LayerConfig:
     drop_tokens: bool
     act: str
     aux_loss_weight: float = 0.0
+    gate_temperature: float = 1.0   # p = softmax(logits / T) (reading R10)
+    aux_loss_type: str = "load"     # "load" | "std"
 
 
 def route(logits: np.ndarray, cfg: LayerConfig) -> dict:
     """Gate stages after the logits: softmax, top-k, weights, slots, l_aux."""
     S, E = logits.shape
-    probs = softmax(logits)
+    probs = softmax(np.asarray(logits, np.float64) / cfg.gate_temperature)
     idx = topk_experts(logits, cfg.k)
     w = gate_weights(probs, idx)
     cap = capacity(S, E, cfg.k, cfg.capacity_factor, cfg.min_capacity,
                    cfg.drop_tokens)
     rt = assign_slots(idx, E, cap)
     return {"logits": np.asarray(logits, np.float64), "probs": probs,
-            "weights": w, "routing": rt, "l_aux": aux_loss(probs, idx)}
+            "weights": w, "routing": rt, "l_aux": aux_loss(probs, idx, cfg.aux_loss_type)}
 
 
 def forward(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, logit_bias=None,
@@ -356,7 +373,7 @@ def dense_mixture(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, logit_bias=None):
     ``drop_tokens`` is false."""
     x = np.asarray(x, np.float64)
     lg = gate_logits(x, w_gate, logit_bias)
-    p = softmax(lg)
+    p = softmax(lg / cfg.gate_temperature)
     idx = topk_experts(lg, cfg.k)
     w = gate_weights(p, idx)
     S, E = lg.shape
@@ -467,10 +484,18 @@ def backward(cfg: LayerConfig, fwd: dict, x, w_gate, w1, w2, dy) -> dict:
         dp[rows, rt.idx[:, 0]] += p2 * (dw[:, 0] - dw[:, 1]) / P2
         dp[rows, rt.idx[:, 1]] += p1 * (dw[:, 1] - dw[:, 0]) / P2
     if cfg.aux_loss_weight != 0.0:
-        first = np.bincount(rt.idx[:, 0], minlength=E).astype(np.float64)
-        dp += cfg.aux_loss_weight * E * first[None, :] / float(S * S)
+        if cfg.aux_loss_type == "std":
+            # d std(u) / d p[s,e] = (u_e - mean u) / (E * std u) * 1/S
+            u = p.mean(axis=0)
+            sd = np.sqrt(np.mean((u - u.mean()) ** 2))
+            if sd > 0.0:
+                dp += cfg.aux_loss_weight * ((u - u.mean()) / (E * S * sd))[None, :]
+        else:
+            first = np.bincount(rt.idx[:, 0], minlength=E).astype(np.float64)
+            dp += cfg.aux_loss_weight * E * first[None, :] / float(S * S)
 
-    dlogits = p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+    # p = softmax(logits / T): the logits' gradient carries the 1/T
+    dlogits = p * (dp - np.sum(dp * p, axis=1, keepdims=True)) / cfg.gate_temperature
     dw_gate = dlogits.T @ x
     dx = dlogits @ w_gate
     for s in range(S):
@@ -491,7 +516,7 @@ def loss(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, dy, logit_bias=None,
     a token between experts."""
     x = np.asarray(x, np.float64)
     lg = gate_logits(x, w_gate, logit_bias)
-    p = softmax(lg)
+    p = softmax(lg / cfg.gate_temperature)
     if routing_from is None:
         g = route(lg, cfg)
         rt, idx = g["routing"], g["routing"].idx
@@ -504,5 +529,5 @@ def loss(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, dy, logit_bias=None,
     y = combine(out, rt, w, x.shape[1])
     val = float(np.sum(np.asarray(dy, np.float64) * y))
     if cfg.aux_loss_weight != 0.0:
-        val += cfg.aux_loss_weight * aux_loss(p, idx)
+        val += cfg.aux_loss_weight * aux_loss(p, idx, cfg.aux_loss_type)
     return val

@@ -39,7 +39,7 @@ def inputs_for(wl: Workload):
 def oracle_cfg(wl: Workload) -> O.LayerConfig:
     return O.LayerConfig(wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k,
                          wl.capacity_factor, wl.min_capacity, wl.drop_tokens, wl.act,
-                         wl.aux_loss_weight)
+                         wl.aux_loss_weight, wl.gate_temperature, wl.aux_loss_type)
 
 
 class GpuRun:

@@ -131,6 +131,32 @@ def test_weights_k1_is_raw_probability():
     assert abs(w[0, 0] - 0.75) < 1e-15
 
 
+def test_gate_temperature_softmax_and_routing():
+    """p = softmax(logits / T) (scipy), the top-k choice is the T = 1 choice,
+    and the k=2 weights are the selected probabilities renormalised."""
+    rng = np.random.default_rng(31)
+    lg = rng.standard_normal((40, 6)) * 2.0
+    for T in (0.5, 2.0):
+        c = cfg(40, 8, 8, 6, 2, cf=2.0)
+        c.gate_temperature = T
+        g = O.route(lg, c)
+        assert np.allclose(g["probs"], scipy_softmax(lg / T, axis=1), rtol=1e-13, atol=1e-15)
+        g1 = O.route(lg, cfg(40, 8, 8, 6, 2, cf=2.0))
+        assert np.array_equal(g["routing"].idx, g1["routing"].idx)
+        ps = np.take_along_axis(scipy_softmax(lg / T, axis=1), g["routing"].idx, axis=1)
+        assert np.allclose(g["weights"], ps / ps.sum(axis=1, keepdims=True), rtol=1e-13)
+
+
+def test_std_balance_loss_hand_worked():
+    """usage u = mean_s p = (0.7, 0.3): population std 0.2, l_aux = 0.2 + 1e-6;
+    uniform probabilities give std 0, l_aux = 1e-6."""
+    p = np.array([[0.9, 0.1], [0.5, 0.5]])
+    idx = np.array([[0], [0]])
+    assert abs(O.aux_loss(p, idx, "std") - (0.2 + 1e-6)) < 1e-15
+    u = np.full((5, 4), 0.25)
+    assert O.aux_loss(u, np.zeros((5, 1), np.int64), "std") == 1e-6
+
+
 def test_aux_loss_closed_forms():
     # uniform probabilities -> 1 whatever the first choices are
     assert abs(O.aux_loss(np.full((10, 4), 0.25), np.zeros((10, 1), np.int64)) - 1.0) < 1e-15
@@ -345,23 +371,31 @@ def test_no_drop_equals_dense_mixture(k):
 # --------------------------------------------------------------------------
 # backward: central finite differences with routing held fixed
 # --------------------------------------------------------------------------
-def _fd_case(k, aux, drop):
+def _fd_case(k, aux, drop, temp=1.0, aux_type="load", per_token=False):
     rng = np.random.default_rng(20 + 2 * k + int(drop))
     S, d, f, E = 7, 4, 5, 4
     c = cfg(S, d, f, E, k, cf=0.5 if drop else 1.0, min_cap=1, drop=drop, aux=aux)
+    c.gate_temperature, c.aux_loss_type = temp, aux_type
     x = rng.standard_normal((S, d))
     wg = rng.standard_normal((E, d)) * 0.7
     w1, b1 = rng.standard_normal((E, f, d)) * 0.5, rng.standard_normal((E, f)) * 0.3
     w2, b2 = rng.standard_normal((E, d, f)) * 0.5, rng.standard_normal((E, d)) * 0.3
     bias = np.array([0.0, 0.4, 0.2, -30.0])     # expert 3 is never chosen
     dy = rng.standard_normal((S, d))
+    if per_token:                                # noisy gating: per-token logit noise
+        bias = bias[None, :] + 0.3 * rng.standard_normal((S, E))
     return c, x, wg, w1, b1, w2, b2, bias, dy
 
 
-@pytest.mark.parametrize("k,aux,drop", [(1, 0.0, True), (2, 0.0, True), (2, 0.01, True),
-                                        (2, 0.3, False), (1, 0.3, False)])
-def test_backward_finite_differences(k, aux, drop):
-    c, x, wg, w1, b1, w2, b2, bias, dy = _fd_case(k, aux, drop)
+@pytest.mark.parametrize("k,aux,drop,temp,aux_type,per_token", [
+    (1, 0.0, True, 1.0, "load", False), (2, 0.0, True, 1.0, "load", False),
+    (2, 0.01, True, 1.0, "load", False), (2, 0.3, False, 1.0, "load", False),
+    (1, 0.3, False, 1.0, "load", False),
+    # gating variants: temperature, the std balance loss, per-token noise
+    (2, 0.3, True, 0.5, "std", True), (1, 0.3, False, 2.0, "std", False),
+    (2, 0.05, True, 0.5, "load", True)])
+def test_backward_finite_differences(k, aux, drop, temp, aux_type, per_token):
+    c, x, wg, w1, b1, w2, b2, bias, dy = _fd_case(k, aux, drop, temp, aux_type, per_token)
     fwd = O.forward(c, x, wg, w1, b1, w2, b2, logit_bias=bias)
     rt = fwd["routing"]
     if drop:
