@@ -165,6 +165,7 @@ def run_gpu(args):
     inp_cpu = make_inputs(wl)
     d = inp_cpu.to(dev)
     bufs = L.alloc_buffers(cfg, dev)
+    bufs["logits"] = None      # optional output of the gate; nothing downstream reads it
     ws = L.alloc_workspace(cfg, dev)
     y = torch.empty_like(d.x)
     st = torch.cuda.current_stream()
@@ -276,7 +277,7 @@ def run_gpu(args):
     def gbs(nbytes, ms_):
         return nbytes / (ms_ * 1e-3) / 1e9
 
-    gate_bytes = S * dm * eb + E * dm * eb + S * E * 4 + S * k * 12
+    gate_bytes = S * dm * eb + E * dm * eb + S * k * 12 + R * 4
     disp_bytes = S * dm * eb + R * dm * eb + S * k * 8
     comb_bytes = R * dm * eb + S * dm * eb + S * k * 12
     stages = {
@@ -455,6 +456,7 @@ def decode_step(args, dev, max_over_ranks, world):
     cfg = N.config_from_workload(wl)
     d = make_inputs(wl).to(dev)
     bufs = L.alloc_buffers(cfg, dev)
+    bufs["logits"] = None
     ws = L.alloc_workspace(cfg, dev)
     y = torch.empty_like(d.x)
     st = torch.cuda.current_stream()

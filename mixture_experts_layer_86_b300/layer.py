@@ -119,6 +119,8 @@ class HostPipeline:
                        "bufs": alloc_buffers(cfg, device),
                        "ev_in": torch.cuda.Event(), "ev_comp": torch.cuda.Event(),
                        "ev_out": torch.cuda.Event(), "used": False} for _ in range(2)]
+        for sl in self.slots:
+            sl["bufs"]["logits"] = None    # the gate's optional output; never copied out
         self.workspace = alloc_workspace(cfg, device)
         self.s_in = torch.cuda.Stream(device)
         self.s_comp = torch.cuda.Stream(device)

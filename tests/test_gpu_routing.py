@@ -119,3 +119,23 @@ def test_gate_routing_beyond_one_wave(S):
     assert np.allclose(f64(b["probs"]), g["probs"], rtol=2e-6, atol=1e-8)
     assert abs(float(b["l_aux"].item()) - g["l_aux"]) <= 1e-5 * abs(g["l_aux"])
     assert N.moe_get_device_error() == 0
+
+
+@pytest.mark.parametrize("S", [8192, 8449, 12000])
+@pytest.mark.parametrize("base", ["e8_bf16", "tiny_fp32"])
+def test_routing_scan_256_experts(base, S):
+    """The routing scan at the widest expert count: with E = 256, k = 2 the
+    512 count columns and 256 probability columns leave only 2 and 4 thread
+    groups per column, each summing a run of 128-token CTAs.  8192 tokens
+    (64 CTAs), 8449 (67, one token in the last CTA) and 12000 (94, ragged);
+    routing must match the oracle on the GPU's own logits."""
+    wl = WORKLOADS[base].scaled(S, bias_std=0.05)
+    wl = type(wl)(**{**wl.__dict__, "num_experts": 256, "k": 2, "hidden_size": 256,
+                     "ffn_size": 64, "name": f"scan256_{base}_S{S}"})
+    run = GpuRun(wl, training=True)
+    g = run.oracle_route()
+    check_routing_equal(run, g)
+    b = run.bufs
+    assert np.allclose(f64(b["topk_w"]), g["weights"], rtol=2e-6, atol=1e-7)
+    assert abs(float(b["l_aux"].item()) - g["l_aux"]) <= 1e-5 * abs(g["l_aux"])
+    assert N.moe_get_device_error() == 0
