@@ -45,6 +45,8 @@ R6  A token whose every slot is dropped contributes y_s = 0 (no residual).
 R7  "GeLU" without qualifier is the tanh form.
 R8  PR-MoE's residual expert (use_residual=True) is combined with the MoE
     output by a sum, y = MoE(x) + MLP(x); the page gives no mixing formula.
+    The other reading offered: a learned per-token two-way mix,
+    c = softmax(x W_c^T + b_c) over 2 entries, y = c0 MoE(x) + c1 MLP(x).
 R9  The std-based balance loss lambda * (std(usage_prob) + 1e-6) reads
     usage_prob[e] as mean_s p[s,e] (the differentiable usage), with the
     population std over experts.
@@ -396,17 +398,34 @@ def residual_mlp(x, rw1, rb1, rw2, rb2, act: str) -> np.ndarray:
     return h @ np.asarray(rw2, np.float64).T + np.asarray(rb2, np.float64)
 
 
+def residual_coef(x, coef_w, coef_b) -> np.ndarray:
+    """Per-token mixing weights of the two branches (reading R8, second
+    form): c[s] = softmax over 2 of (x_s W_c^T + b_c); W_c [2,d], b_c [2]."""
+    z = np.asarray(x, np.float64) @ np.asarray(coef_w, np.float64).T + np.asarray(coef_b, np.float64)
+    z = z - z.max(axis=1, keepdims=True)
+    ez = np.exp(z)
+    return ez / ez.sum(axis=1, keepdims=True)
+
+
 def forward_residual(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
-                     logit_bias=None, logits: Optional[np.ndarray] = None) -> dict:
+                     logit_bias=None, logits: Optional[np.ndarray] = None,
+                     coef_w=None, coef_b=None) -> dict:
     """The PR-MoE layer.  The page names the residual connection but gives no
     mixing formula; reading R8: the connection is a sum,
-    y = MoE(x) + MLP(x).  Returns ``forward``'s dict with ``y`` replaced and
-    ``y_moe`` / ``residual`` added."""
+    y = MoE(x) + MLP(x), or, when the mixing weights W_c [2,d], b_c [2] are
+    given, y = c0 MoE(x) + c1 MLP(x) with c = residual_coef(x, W_c, b_c).
+    Returns ``forward``'s dict with ``y`` replaced and ``y_moe`` /
+    ``residual`` (and ``coef``) added."""
     g = forward(cfg, x, w_gate, w1, b1, w2, b2, logit_bias=logit_bias, logits=logits)
     r = residual_mlp(x, rw1, rb1, rw2, rb2, cfg.act)
     g["y_moe"] = g["y"]
     g["residual"] = r
-    g["y"] = g["y_moe"] + r
+    if coef_w is None:
+        g["y"] = g["y_moe"] + r
+    else:
+        c = residual_coef(x, coef_w, coef_b)
+        g["coef"] = c
+        g["y"] = c[:, 0:1] * g["y_moe"] + c[:, 1:2] * r
     return g
 
 

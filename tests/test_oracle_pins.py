@@ -428,3 +428,37 @@ def test_backward_finite_differences(k, aux, drop, temp, aux_type, per_token):
     assert rt.kept[3] == 0
     for key in ("dw1", "db1", "dw2", "db2"):
         assert np.all(g[key][3] == 0.0)
+
+
+def test_residual_learned_mix_coefficient():
+    """PR-MoE with learned per-token mixing (reading R8, second form): the two
+    weights are a logistic sigmoid of the difference of two torch Linear
+    outputs; zero mixing weights halve the sum form; a saturated bias gives
+    the plain layer or the MLP alone."""
+    from scipy.special import expit
+    rng = np.random.default_rng(23)
+    S, d, f, E = 25, 6, 8, 4
+    c = cfg(S, d, f, E, 2, cf=1.0, min_cap=1)
+    x = rng.standard_normal((S, d))
+    wg = rng.standard_normal((E, d))
+    w1, b1 = rng.standard_normal((E, f, d)), rng.standard_normal((E, f))
+    w2, b2 = rng.standard_normal((E, d, f)), rng.standard_normal((E, d))
+    rw1, rb1 = rng.standard_normal((f, d)), rng.standard_normal(f)
+    rw2, rb2 = rng.standard_normal((d, f)), rng.standard_normal(d)
+    cw, cb = rng.standard_normal((2, d)), rng.standard_normal(2)
+    g = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, rw2, rb2, coef_w=cw, coef_b=cb)
+    z = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(cw),
+                                   torch.from_numpy(cb)).numpy()
+    c0 = expit(z[:, 0] - z[:, 1])
+    assert np.allclose(g["coef"][:, 0], c0, rtol=1e-13, atol=1e-15)
+    assert np.allclose(g["coef"][:, 1], 1.0 - c0, rtol=1e-12, atol=1e-15)
+    plain = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, rw2, rb2)
+    assert np.allclose(g["y"], c0[:, None] * plain["y_moe"] + (1.0 - c0)[:, None] * plain["residual"],
+                       rtol=1e-12, atol=1e-12)
+    half = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
+                              coef_w=np.zeros((2, d)), coef_b=np.zeros(2))
+    assert np.allclose(half["y"], 0.5 * plain["y"], rtol=1e-14, atol=1e-14)
+    for bias, want in (([40.0, -40.0], plain["y_moe"]), ([-40.0, 40.0], plain["residual"])):
+        sat = O.forward_residual(c, x, wg, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
+                                 coef_w=np.zeros((2, d)), coef_b=np.array(bias))
+        assert np.allclose(sat["y"], want, rtol=1e-12, atol=1e-12)
