@@ -409,37 +409,48 @@ def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
 
     from mixture_experts_layer_86_b300 import _native as N
     from mixture_experts_layer_86_b300 import layer as L
-    from mixture_experts_layer_86_b300.inputs import make_residual_weights
+    from mixture_experts_layer_86_b300.inputs import make_residual_mix, make_residual_weights
 
     rw = [t.to(dev) for t in make_residual_weights(wl)]
+    mix_w, mix_b = [t.to(dev) for t in make_residual_mix(wl)]
     bufs = L.alloc_buffers(cfg, dev)
+    bufs["logits"] = None
     ws = L.alloc_workspace(cfg, dev)
     y = torch.empty_like(d.x)
     res_h = torch.empty((wl.num_tokens, wl.ffn_size), dtype=d.x.dtype, device=dev)
     res_out = torch.empty_like(d.x)
+    mix = torch.empty((wl.num_tokens, 2), dtype=torch.float32, device=dev)
     st = torch.cuda.current_stream()
-
-    def step():
-        N.moe_forward_residual(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, *rw, y,
-                               bufs, res_h, res_out, ws, st)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
     steps = max(1, min(args.steps, 100))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(steps):
-        step()
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1))
+
+    def timed(learned):
+        def step():
+            N.moe_forward_residual(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, *rw,
+                                   y, bufs, res_h, res_out, ws, st,
+                                   mix_w=mix_w if learned else None,
+                                   mix_b=mix_b if learned else None, mix=mix if learned else None)
+
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1))
+
+    ms = timed(False)
+    ms_mix = timed(True)
     R = int(bufs["expert_offsets"][-1].item())
     flops = 4.0 * (R + wl.num_tokens) * wl.hidden_size * wl.ffn_size
     return {"workload": workload_desc(wl).replace("MoE layer forward", "PR-MoE forward (+ dense MLP)"),
             "value": world * wl.num_tokens * steps / (ms * 1e-3), "unit": "tokens/s",
             "ms_per_step": ms / steps, "steps": steps,
-            "expert_and_mlp_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
+            "expert_and_mlp_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12,
+            "learned_mix": {"value": world * wl.num_tokens * steps / (ms_mix * 1e-3),
+                            "unit": "tokens/s", "ms_per_step": ms_mix / steps}}
 
 
 def decode_step(args, dev, max_over_ranks, world):

@@ -244,23 +244,29 @@ moe_status moe_forward(const moe_config *cfg, const void *x,
                        moe_stream_t stream);
 
 /* The forward pass with PR-MoE's residual expert (deepspeed.moe overview
- * §2.3 / §3.3, MoE(..., use_residual=True): "a fixed MLP combined with the
- * dynamic experts").  The page gives no mixing formula; the residual
- * connection is read as a sum:
- *   y = MoE(x) + MLP(x),   MLP(x) = act(x rw1^T + rb1) rw2^T + rb2
- * with the MLP (the same shape and activation as one expert) applied to
- * every token.  rw1: [f,d]; rb1: [f]; rw2: [d,f]; rb2: [d] (T);
- * res_h: [S,f] T and res_out: [S,d] T receive the MLP's activation and
- * output (caller-owned scratch); the other arguments are moe_forward's.
- * The MLP's output is added inside the combine, in fp32. */
+ * §2.3 / §3.3, MoE(..., use_residual=True), where a fixed dense MLP works
+ * beside the routed experts).  The page does not say how the two outputs
+ * are mixed; two readings are offered:
+ *   mix_w == NULL:  y = MoE(x) + MLP(x)                       (a sum)
+ *   mix_w != NULL:  c[s] = softmax over 2 of (x[s] mix_w^T + mix_b),
+ *                   y[s] = c[s,0] MoE(x)[s] + c[s,1] MLP(x)[s]
+ * with MLP(x) = act(x rw1^T + rb1) rw2^T + rb2 (the shape and activation of
+ * one expert) applied to every token.  rw1: [f,d]; rb1: [f]; rw2: [d,f];
+ * rb2: [d]; mix_w: [2,d]; mix_b: [2] (all T).  mix: [S,2] fp32 receives c
+ * (required with mix_w; mix_b and mix must both be NULL without it, else
+ * MOE_ERR_INVALID_ARG).  res_h: [S,f] T and res_out: [S,d] T receive the
+ * MLP's activation and output (caller-owned scratch); the other arguments
+ * are moe_forward's.  The MLP's output is mixed in inside the combine, in
+ * fp32; c is computed with fp32 dot products. */
 moe_status moe_forward_residual(const moe_config *cfg, const void *x,
                                 const void *w_gate, const float *logit_bias,
                                 const void *w1, const void *b1, const void *w2,
                                 const void *b2, const void *rw1, const void *rb1,
-                                const void *rw2, const void *rb2, void *y,
-                                const moe_buffers *buf, void *res_h, void *res_out,
-                                void *workspace, size_t workspace_bytes,
-                                moe_stream_t stream);
+                                const void *rw2, const void *rb2,
+                                const void *mix_w, const void *mix_b, float *mix,
+                                void *y, const moe_buffers *buf, void *res_h,
+                                void *res_out, void *workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
 
 /* Backward of L = <dy, y> + aux_loss_weight * l_aux with the routing held
  * fixed (DeepSeek-MoE page §3.1 TopKRouter: the gradient reaches only the

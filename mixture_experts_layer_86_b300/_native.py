@@ -63,7 +63,7 @@ _SIGS = {
     "moe_combine": (c_int, [POINTER(MoeConfig)] + [_P] * 6 + [_P]),
     "moe_forward": (c_int, [POINTER(MoeConfig)] + [_P] * 8 + [POINTER(MoeBuffers), _P,
                                                              c_size_t, _P]),
-    "moe_forward_residual": (c_int, [POINTER(MoeConfig)] + [_P] * 12 + [POINTER(MoeBuffers)]
+    "moe_forward_residual": (c_int, [POINTER(MoeConfig)] + [_P] * 15 + [POINTER(MoeBuffers)]
                              + [_P] * 3 + [c_size_t, _P]),
     "moe_backward": (c_int, [POINTER(MoeConfig)] + [_P] * 4 + [POINTER(MoeBuffers)] + [_P] * 8
                      + [c_size_t, _P]),
@@ -211,12 +211,13 @@ def moe_forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, y, bufs, workspace, 
 
 
 def moe_forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, rb2, y,
-                         bufs, res_h, res_out, workspace, stream=None):
+                         bufs, res_h, res_out, workspace, stream=None, mix_w=None, mix_b=None,
+                         mix=None):
     b = bufs if isinstance(bufs, MoeBuffers) else buffers_struct(bufs)
     _check("moe_forward_residual", _lib.moe_forward_residual(
         ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(w1), _ptr(b1),
-        _ptr(w2), _ptr(b2), _ptr(rw1), _ptr(rb1), _ptr(rw2), _ptr(rb2), _ptr(y), ctypes.byref(b),
-        _ptr(res_h), _ptr(res_out), _ptr(workspace),
+        _ptr(w2), _ptr(b2), _ptr(rw1), _ptr(rb1), _ptr(rw2), _ptr(rb2), _ptr(mix_w), _ptr(mix_b),
+        _ptr(mix), _ptr(y), ctypes.byref(b), _ptr(res_h), _ptr(res_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -387,15 +387,22 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_gate,
 moe_status moe_forward_residual(const moe_config *cfg, const void *x, const void *w_gate,
                                 const float *logit_bias, const void *w1, const void *b1,
                                 const void *w2, const void *b2, const void *rw1, const void *rb1,
-                                const void *rw2, const void *rb2, void *y, const moe_buffers *buf,
+                                const void *rw2, const void *rb2, const void *mix_w,
+                                const void *mix_b, float *mix, void *y, const moe_buffers *buf,
                                 void *res_h, void *res_out, void *workspace,
                                 size_t workspace_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
   if (!buf || !ok_ptr(y) || !ok_ptr(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
       !ok_opt(buf->h_pre) || !ok_ptr(w1) || !ok_ptr(b1) || !ok_ptr(w2) || !ok_ptr(b2) ||
       !ok_ptr(rw1) || !ok_ptr(rb1) || !ok_ptr(rw2) || !ok_ptr(rb2) || !ok_ptr(res_h) ||
-      !ok_ptr(res_out))
+      !ok_ptr(res_out) || !ok_opt(mix_w))
     return MOE_ERR_INVALID_ARG;
+  // the learned mix takes all three of its arguments, the sum none of them
+  if (mix_w ? (!ok_ptr(mix_b) || !ok_ptr(mix)) : (mix_b != nullptr || mix != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (mix_w)
+    MOE_CUDA(launch_residual_mix(x, cfg->dtype, cfg->num_tokens, cfg->hidden_size, mix_w, mix_b,
+                                 mix, stream));
   MOE_TRY(moe_gate_topk(cfg, x, w_gate, logit_bias, buf->logits, buf->probs, buf->topk_idx,
                         buf->topk_w, buf->slot, buf->routed_cnt, buf->kept_cnt,
                         buf->expert_offsets, buf->row_src, buf->l_aux, workspace, workspace_bytes,
@@ -407,7 +414,7 @@ moe_status moe_forward_residual(const moe_config *cfg, const void *x, const void
   MOE_TRY(dense_mlp(cfg, x, rw1, rb1, rw2, rb2, res_h, res_out, stream));
   return cuda_status(launch_combine(buf->out_disp, cfg->dtype, cfg->num_tokens, cfg->hidden_size,
                                     cfg->k, buf->topk_idx, buf->slot, buf->expert_offsets,
-                                    buf->topk_w, y, stream, res_out));
+                                    buf->topk_w, y, stream, res_out, mix));
 }
 
 moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate, const void *w1,

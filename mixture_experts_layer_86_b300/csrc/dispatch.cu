@@ -48,13 +48,16 @@ dispatch_kernel(const uint4 *__restrict__ x, int64_t S, int nvec, int k,
   }
 }
 
-// y[s] = res[s] (if res is set) + sum_j w[s,j] * out[row(s,j)]
+// y[s] = res[s] (if res is set) + sum_j w[s,j] * out[row(s,j)]; with the
+// per-token mixing weights mix[s] = (c0, c1) set:
+// y[s] = c1 * res[s] + c0 * sum_j w[s,j] * out[row(s,j)]
 template <typename T>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
                const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
                const int32_t *__restrict__ offsets, const float *__restrict__ w,
-               const uint4 *__restrict__ res, uint4 *__restrict__ y) {
+               const uint4 *__restrict__ res, const float2 *__restrict__ mix,
+               uint4 *__restrict__ y) {
   griddep_begin();
   using V = Vec<T>;
   const int lane = threadIdx.x & 31;
@@ -62,12 +65,17 @@ combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
   if (s >= S) return;
   const int64_t r0 = row_of(idx, slot, offsets, s * k);
   const int64_t r1 = k == 2 ? row_of(idx, slot, offsets, s * k + 1) : -1;
-  const float w0 = w[s * k];
-  const float w1 = k == 2 ? w[s * k + 1] : 0.0f;
+  const float2 cm = mix ? mix[s] : make_float2(1.0f, 1.0f);
+  const float w0 = cm.x * w[s * k];
+  const float w1 = k == 2 ? cm.x * w[s * k + 1] : 0.0f;
   for (int c = lane; c < nvec; c += 32) {
     float acc[V::kN], t[V::kN];
     if (res) {
       V::to_f32(ld_stream(res + s * nvec + c), acc);
+      if (mix) {
+#pragma unroll
+        for (int i = 0; i < V::kN; ++i) acc[i] *= cm.y;
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < V::kN; ++i) acc[i] = 0.0f;
@@ -83,6 +91,41 @@ combine_kernel(const uint4 *__restrict__ out, int64_t S, int nvec, int k,
       for (int i = 0; i < V::kN; ++i) acc[i] = fmaf(w1, t[i], acc[i]);
     }
     y[s * nvec + c] = V::from_f32(acc);
+  }
+}
+
+// PR-MoE's learned mixing weights: mix[s] = softmax over two of
+// (x[s] . cw[j] + cb[j]), j = 0 (the experts) and 1 (the dense MLP); one
+// warp per token, x and cw read in 16-byte vectors, fp32 dot products.
+template <typename T>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+residual_mix_kernel(const uint4 *__restrict__ x, int64_t S, int nvec,
+                    const uint4 *__restrict__ cw, const T *__restrict__ cb,
+                    float2 *__restrict__ mix) {
+  griddep_begin();
+  using V = Vec<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (s >= S) return;
+  float z0 = 0.0f, z1 = 0.0f;
+  for (int c = lane; c < nvec; c += 32) {
+    float xv[V::kN], a[V::kN], b[V::kN];
+    V::to_f32(ld_stream(x + s * nvec + c), xv);
+    V::to_f32(cw[c], a);
+    V::to_f32(cw[nvec + c], b);
+#pragma unroll
+    for (int i = 0; i < V::kN; ++i) {
+      z0 = fmaf(xv[i], a[i], z0);
+      z1 = fmaf(xv[i], b[i], z1);
+    }
+  }
+  z0 = warp_sum(z0) + float(cb[0]);
+  z1 = warp_sum(z1) + float(cb[1]);
+  if (lane == 0) {
+    const float m = fmaxf(z0, z1);
+    const float e0 = expf(z0 - m), e1 = expf(z1 - m);
+    const float inv = 1.0f / (e0 + e1);
+    mix[s] = make_float2(e0 * inv, e1 * inv);
   }
 }
 
@@ -261,16 +304,32 @@ cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
 
 cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d, int k,
                            const int32_t *idx, const int32_t *slot, const int32_t *offsets,
-                           const float *w, void *y, cudaStream_t st, const void *res) {
+                           const float *w, void *y, cudaStream_t st, const void *res,
+                           const float *mix) {
   if (S == 0) return cudaSuccess;
   const int nvec = d * elem_bytes(dtype) / 16;
+  auto *m2 = reinterpret_cast<const float2 *>(mix);
   if (dtype == MOE_F32)
     return launch_k(combine_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st,
                     static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-                    static_cast<const uint4 *>(res), static_cast<uint4 *>(y));
+                    static_cast<const uint4 *>(res), m2, static_cast<uint4 *>(y));
   return launch_k(combine_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st,
                   static_cast<const uint4 *>(out_disp), S, nvec, k, idx, slot, offsets, w,
-                  static_cast<const uint4 *>(res), static_cast<uint4 *>(y));
+                  static_cast<const uint4 *>(res), m2, static_cast<uint4 *>(y));
+}
+
+cudaError_t launch_residual_mix(const void *x, int dtype, int64_t S, int d, const void *cw,
+                                const void *cb, float *mix, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  const int nvec = d * elem_bytes(dtype) / 16;
+  auto *m2 = reinterpret_cast<float2 *>(mix);
+  if (dtype == MOE_F32)
+    return launch_k(residual_mix_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st,
+                    static_cast<const uint4 *>(x), S, nvec, static_cast<const uint4 *>(cw),
+                    static_cast<const float *>(cb), m2);
+  return launch_k(residual_mix_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st,
+                  static_cast<const uint4 *>(x), S, nvec, static_cast<const uint4 *>(cw),
+                  static_cast<const __nv_bfloat16 *>(cb), m2);
 }
 
 cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, int64_t S,

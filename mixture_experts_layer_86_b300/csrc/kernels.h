@@ -121,11 +121,18 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);
 cudaError_t launch_dispatch(const void *x, int dtype, int64_t S, int d, int k,
                             const int32_t *idx, const int32_t *slot,
                             const int32_t *offsets, void *x_disp, cudaStream_t st);
-// y[s] = res[s] (when res is not null) + sum_j w[s,j] * out_disp[row(s,j)]
+// y[s] = res[s] (when res is not null) + sum_j w[s,j] * out_disp[row(s,j)];
+// with mix ([S,2] fp32) set as well: y[s] = mix[s,1] res[s] + mix[s,0] sum_j ...
 cudaError_t launch_combine(const void *out_disp, int dtype, int64_t S, int d,
                            int k, const int32_t *idx, const int32_t *slot,
                            const int32_t *offsets, const float *w, void *y,
-                           cudaStream_t st, const void *res = nullptr);
+                           cudaStream_t st, const void *res = nullptr,
+                           const float *mix = nullptr);
+// mix[s] = softmax over two of (x[s] . cw[j] + cb[j]); cw [2,d], cb [2] in
+// the layer dtype, mix [S,2] fp32.
+cudaError_t launch_residual_mix(const void *x, int dtype, int64_t S, int d,
+                                const void *cw, const void *cb, float *mix,
+                                cudaStream_t st);
 
 // ------------------------------------------------ backward helpers
 // dO[row] = w * dY[s], dw[s,j] = <dY[s], out[row]> (0 when dropped).

@@ -169,6 +169,17 @@ def make_residual_weights(wl: Workload):
     return rw1, rb1, rw2, rb2
 
 
+def make_residual_mix(wl: Workload):
+    """Weights of PR-MoE's learned two-way mix for a workload: a CPU
+    generator seeded with seed + 2000 draws, in float32, mix_w ~ N(0, 1/d)
+    [2, d] then mix_b ~ N(0, 0.5^2) [2], cast to the layer dtype."""
+    g = torch.Generator().manual_seed(wl.seed + 2000)
+    d, dt = wl.hidden_size, wl.torch_dtype
+    mix_w = (torch.randn((2, d), generator=g, dtype=torch.float32) / math.sqrt(d)).to(dt)
+    mix_b = (torch.randn((2,), generator=g, dtype=torch.float32) * 0.5).to(dt)
+    return mix_w, mix_b
+
+
 def make_gate_inputs(wl: Workload):
     """x, W_g and the logit bias exactly as make_inputs draws them (the first
     two draws of the recipe), without drawing the expert weights."""

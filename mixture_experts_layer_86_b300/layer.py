@@ -61,11 +61,13 @@ def forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, bufs=None, workspace=Non
 
 
 def forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, rb2,
-                     bufs=None, workspace=None, y=None, stream=None):
+                     bufs=None, workspace=None, y=None, stream=None, mix_w=None, mix_b=None):
     """PR-MoE layer (``use_residual=True``): y = MoE(x) + MLP(x) with the
-    dense MLP weights rw1 [f,d], rb1 [f], rw2 [d,f], rb2 [d].  Returns
-    (y, l_aux, expert_count, state); state also holds the MLP's activation
-    ("res_h") and output ("res_out")."""
+    dense MLP weights rw1 [f,d], rb1 [f], rw2 [d,f], rb2 [d]; with the mixing
+    weights mix_w [2,d], mix_b [2] given, y = c0 MoE(x) + c1 MLP(x) with
+    c = softmax(x mix_w^T + mix_b) per token.  Returns (y, l_aux,
+    expert_count, state); state also holds the MLP's activation ("res_h"),
+    output ("res_out") and, with the mix, c ("mix", [S,2] fp32)."""
     dev = x.device
     if bufs is None:
         bufs = alloc_buffers(cfg, dev)
@@ -76,9 +78,13 @@ def forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, 
     dt = torch_dtype(cfg)
     res_h = torch.empty((cfg.num_tokens, cfg.ffn_size), dtype=dt, device=dev)
     res_out = torch.empty((cfg.num_tokens, cfg.hidden_size), dtype=dt, device=dev)
+    mix = None
+    if mix_w is not None:
+        mix = torch.empty((cfg.num_tokens, 2), dtype=torch.float32, device=dev)
     N.moe_forward_residual(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, rw1, rb1, rw2, rb2, y,
-                           bufs, res_h, res_out, workspace, stream)
-    state = dict(bufs, res_h=res_h, res_out=res_out)
+                           bufs, res_h, res_out, workspace, stream, mix_w=mix_w, mix_b=mix_b,
+                           mix=mix)
+    state = dict(bufs, res_h=res_h, res_out=res_out, mix=mix)
     return y, bufs["l_aux"], bufs["kept_cnt"], state
 
 

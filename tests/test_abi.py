@@ -132,3 +132,23 @@ def test_null_misaligned_and_workspace_checks():
                             FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, None) == N.MOE_ERR_WORKSPACE
     bad = N.make_config(64, 32, 64, 4, 3, 1.0, 4, True)
     assert lib.moe_gate_topk(*_gate_args(bad)) == N.MOE_ERR_INVALID_ARG
+
+
+def test_residual_mix_argument_checks():
+    """moe_forward_residual takes the learned mix's three arguments all
+    together or none of them; the checks run before anything is enqueued."""
+    lib = N.library()
+    cfg = N.make_config(64, 32, 64, 4, 1, 1.0, 4, True, "relu", "f32")
+    full = N.MoeBuffers(*([FAKE] * 14))
+
+    def call(mix_w, mix_b, mix):
+        return lib.moe_forward_residual(ctypes.byref(cfg), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                                        FAKE, FAKE, FAKE, FAKE, FAKE, mix_w, mix_b, mix, FAKE,
+                                        ctypes.byref(full), FAKE, FAKE, FAKE, 1 << 40, None)
+
+    assert call(FAKE, FAKE, None) == N.MOE_ERR_INVALID_ARG
+    assert call(FAKE, None, FAKE) == N.MOE_ERR_INVALID_ARG
+    assert call(None, FAKE, None) == N.MOE_ERR_INVALID_ARG
+    assert call(None, None, FAKE) == N.MOE_ERR_INVALID_ARG
+    assert call(MISALIGNED, FAKE, FAKE) == N.MOE_ERR_INVALID_ARG
+    assert call(FAKE, FAKE, MISALIGNED) == N.MOE_ERR_INVALID_ARG
