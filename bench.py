@@ -132,6 +132,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------- replica timing
+def reduce_max(v: float, world: int, device) -> float:
+    """The maximum of v over the ranks of the default process group (v itself
+    on one rank): the job's time is its slowest replica's."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each ran `steps` steps of
+    `tokens_per_step` tokens in `ms` milliseconds (the max over ranks)."""
+    return world * tokens_per_step * steps / (ms * 1e-3)
+
+
 # --------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -154,11 +173,7 @@ def run_gpu(args):
             dist.barrier()
 
     def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, dev)
 
     wl = WORKLOADS[args.workload]
     cfg = N.config_from_workload(wl)
@@ -293,7 +308,7 @@ def run_gpu(args):
     launches_per_step = 7  # gate, scan, assign, dispatch, 2 expert GEMMs, combine
     line = {
         "metric": METRIC,
-        "value": world * S * args.steps / (ms * 1e-3),
+        "value": job_tokens_per_s(world, S, args.steps, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -325,7 +340,7 @@ def run_gpu(args):
         "train_step": train,
         "decode_step": decode,
         "residual_step": residual,
-        "e2e": {"value": world * S * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, S, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": S * dm * eb,
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
                 "ms_per_step": e2e_ms / args.steps,
@@ -396,7 +411,7 @@ def train_step(args, dev, barrier, max_over_ranks, world):
         bw.append(ev[1].elapsed_time(ev[2]))
     flops = 12.0 * R * wl.hidden_size * wl.ffn_size   # expert GEMMs: 4 fwd + 8 bwd
     return {"workload": workload_desc(wl).replace("forward", "forward+backward"),
-            "value": world * wl.num_tokens * steps / (ms * 1e-3), "unit": "tokens/s",
+            "value": job_tokens_per_s(world, wl.num_tokens, steps, ms), "unit": "tokens/s",
             "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
             "fwd_ms": statistics.median(fw), "bwd_ms": statistics.median(bw),
             "expert_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
@@ -446,10 +461,10 @@ def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
     R = int(bufs["expert_offsets"][-1].item())
     flops = 4.0 * (R + wl.num_tokens) * wl.hidden_size * wl.ffn_size
     return {"workload": workload_desc(wl).replace("MoE layer forward", "PR-MoE forward (+ dense MLP)"),
-            "value": world * wl.num_tokens * steps / (ms * 1e-3), "unit": "tokens/s",
+            "value": job_tokens_per_s(world, wl.num_tokens, steps, ms), "unit": "tokens/s",
             "ms_per_step": ms / steps, "steps": steps,
             "expert_and_mlp_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12,
-            "learned_mix": {"value": world * wl.num_tokens * steps / (ms_mix * 1e-3),
+            "learned_mix": {"value": job_tokens_per_s(world, wl.num_tokens, steps, ms_mix),
                             "unit": "tokens/s", "ms_per_step": ms_mix / steps}}
 
 
@@ -511,7 +526,7 @@ def decode_step(args, dev, max_over_ranks, world):
     ffn_bytes = used * (2 * f * dm + f + dm) * 2 + R * (2 * dm + 2 * f) * 2
     peaks, _ = load_peaks()
     gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
-    return {"workload": workload_desc(wl), "value": world * wl.num_tokens * steps / (ms * 1e-3),
+    return {"workload": workload_desc(wl), "value": job_tokens_per_s(world, wl.num_tokens, steps, ms),
             "unit": "tokens/s", "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
             "experts_used": used,
             "expert_ffn": {"ms": ffn_ms, "bytes": ffn_bytes, "GB/s": gbs, "bound": "hbm",
