@@ -438,26 +438,33 @@ def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
     st = torch.cuda.current_stream()
     steps = max(1, min(args.steps, 100))
 
-    def timed(learned):
-        def step():
-            N.moe_forward_residual(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, *rw,
-                                   y, bufs, res_h, res_out, ws, st,
-                                   mix_w=mix_w if learned else None,
-                                   mix_b=mix_b if learned else None, mix=mix if learned else None)
+    def step(learned):
+        N.moe_forward_residual(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, *rw,
+                               y, bufs, res_h, res_out, ws, st,
+                               mix_w=mix_w if learned else None,
+                               mix_b=mix_b if learned else None, mix=mix if learned else None)
 
-        for _ in range(max(args.warmup, 3)):
-            step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(steps):
-            step()
-        e1.record(st)
-        torch.cuda.synchronize()
-        return max_over_ranks(e0.elapsed_time(e1))
-
-    ms = timed(False)
-    ms_mix = timed(True)
+    for _ in range(max(args.warmup, 3)):
+        step(False)
+        step(True)
+    torch.cuda.synchronize()
+    # the two forms run in alternating blocks (ABBA...), so a drift of the
+    # power-capped clock over the run weighs on both alike
+    blocks = 4
+    per_block = max(1, steps // blocks)
+    steps = per_block * blocks
+    total = {False: 0.0, True: 0.0}
+    for b in range(blocks):
+        for learned in ((False, True) if b % 2 == 0 else (True, False)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(per_block):
+                step(learned)
+            e1.record(st)
+            torch.cuda.synchronize()
+            total[learned] += e0.elapsed_time(e1)
+    ms = max_over_ranks(total[False])
+    ms_mix = max_over_ranks(total[True])
     R = int(bufs["expert_offsets"][-1].item())
     flops = 4.0 * (R + wl.num_tokens) * wl.hidden_size * wl.ffn_size
     return {"workload": workload_desc(wl).replace("MoE layer forward", "PR-MoE forward (+ dense MLP)"),
