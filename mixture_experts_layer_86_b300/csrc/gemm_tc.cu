@@ -13,6 +13,11 @@
 // tile's up to 127 -- at ~500 tokens per expert that padding was ~11% of
 // the tensor work.
 //
+// Two kernels share this design.  tc_gemm_pair_kernel (further down) runs
+// it on 2-CTA clusters with tcgen05.mma.cta_group::2 and is the one used on
+// any device with two or more SMs; tc_gemm_kernel, described here, is the
+// single-CTA form of the same tile loop.
+//
 // Tiling: 128 output features x up to 256 tokens per tile, K in 64-element
 // (128 B) slices, 4-stage TMA -> shared memory pipeline with 128-byte
 // swizzle, tcgen05.mma (M=128, N=16..256, K=16) accumulating in TMEM, two
@@ -367,7 +372,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 // instead of 12 KB: with one CTA per SM the 128 x 256 tile needs more
 // shared-memory bandwidth than the SM has, the pair does not.
 //   both CTAs   warp 0: TMA loads of this CTA's halves, completion counted
-//               on the even CTA's `full` barrier; warps 2..5: epilogue of
+//               on the even CTA's `full` barrier; warps 2..9: epilogue of
 //               this CTA's 128 features (its own TMEM), release of the
 //               accumulator on the even CTA's `tempty` barrier
 //   even CTA    warp 1: the pair's MMAs; commits are multicast to the
