@@ -144,15 +144,17 @@ moe_status moe_workspace_size(const moe_config *cfg, int for_backward,
 /* Gate (MoE explainer §3.1 Steps 1-2; DeepSeek-MoE page ch.1 moe_forward and
  * capacity table; deepspeed.moe overview §2.1 drop_tokens / expert_count):
  *   logits = x w_gate^T + logit_bias          (fp32 accumulation)
- *   probs = softmax(logits)
+ *   probs = softmax(logits / T), T = cfg->gate_temperature
  *   topk_idx: arg-max logit, then arg-max of the rest; ties -> lower index
  *   topk_w: k=2 -> p_j / (p_1 + p_2);  k=1 -> p_1
  *   slot: queue position per expert, all first choices in token order before
  *         any second choice; slot >= capacity -> -1 (dropped)
  *   routed_cnt[e], kept_cnt[e], expert_offsets = exclusive scan of kept_cnt,
  *   row_src[offsets[e]+slot] = s*k+j,
- *   l_aux = E * sum_e mean_s(p[s,e]) * (first-choice count of e)/S.
- * x: [S,d] T.  w_gate: [E,d] T.  logit_bias: [E] fp32 or NULL.
+ *   l_aux = E * sum_e mean_s(p[s,e]) * (first-choice count of e)/S, or the
+ *           std form when cfg->aux_loss_type is MOE_AUX_STD.
+ * x: [S,d] T.  w_gate: [E,d] T.  logit_bias: fp32, [E] (or [S,E] when
+ * cfg->logit_bias_per_token), or NULL.
  * logits, probs: [S,E] fp32 or NULL (not written).  Other outputs as in
  * moe_buffers.  workspace: moe_workspace_size(cfg, 0) bytes. */
 moe_status moe_gate_topk(const moe_config *cfg, const void *x,
