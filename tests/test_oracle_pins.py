@@ -104,6 +104,53 @@ def test_exact_tie_cases():
 
 
 # --------------------------------------------------------------------------
+# gate logits
+# --------------------------------------------------------------------------
+def test_gate_logits_against_torch_linear():
+    """logits = x W_g^T + b is torch's Linear layer (the router of the MoE
+    explainer §3.1 Step 1) in float64: without a bias, with one [E] bias
+    shared by every token, and with a per-token [S,E] bias (caller-drawn
+    gate noise) added row by row."""
+    rng = np.random.default_rng(41)
+    S, d, E = 37, 24, 5
+    x = rng.standard_normal((S, d))
+    w = rng.standard_normal((E, d))
+    b = rng.standard_normal(E)
+    B = rng.standard_normal((S, E))
+    tx, tw = torch.from_numpy(x), torch.from_numpy(w)
+    lin = torch.nn.functional.linear
+    assert np.allclose(O.gate_logits(x, w), lin(tx, tw).numpy(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(O.gate_logits(x, w, b), lin(tx, tw, torch.from_numpy(b)).numpy(),
+                       rtol=1e-13, atol=1e-13)
+    per_tok = torch.stack([lin(tx[s], tw, torch.from_numpy(B[s])) for s in range(S)])
+    assert np.allclose(O.gate_logits(x, w, B), per_tok.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_gate_logits_bias_forms_are_local():
+    """A per-token bias moves only its own token's logit; an [E] bias moves
+    that expert's logit of every token by the same amount; the operand is
+    x W_g^T, not x W_g or W_g x (a transposed weight fails the shape or the
+    single-entry check)."""
+    rng = np.random.default_rng(42)
+    S, d, E = 6, 4, 3
+    x = rng.standard_normal((S, d))
+    w = rng.standard_normal((E, d))
+    base = O.gate_logits(x, w)
+    B = np.zeros((S, E))
+    B[4, 1] = 2.5
+    diff = O.gate_logits(x, w, B) - base
+    want = np.zeros((S, E))
+    want[4, 1] = 2.5
+    assert np.allclose(diff, want, rtol=0, atol=1e-14)
+    b = np.array([0.0, -1.0, 0.5])
+    assert np.allclose(O.gate_logits(x, w, b) - base, np.tile(b, (S, 1)), rtol=0, atol=1e-14)
+    # one-hot token and one-hot weight row pick out a single weight entry
+    xo = np.zeros((1, d))
+    xo[0, 3] = 1.0
+    assert np.allclose(O.gate_logits(xo, w)[0], w[:, 3], rtol=0, atol=0)
+
+
+# --------------------------------------------------------------------------
 # softmax / weights / l_aux
 # --------------------------------------------------------------------------
 def test_softmax_matches_scipy():
