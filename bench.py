@@ -1,11 +1,25 @@
-"""Throughput of the MoE layer forward on B300, one JSON line on rank 0.
+"""Throughput of the MoE layer on B300, one JSON line on rank 0.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-configs] [--no-cpu]
 
 A step is one forward pass of the whole layer (gate GEMM, softmax / top-k /
 capacity / slots, dispatch, grouped expert FFN, combine) over one batch of
-synthetic input, through the library's C ABI.  The default workload is the
-64-expert layer (S=16384, d=2048, E=64, f=5120, top-2, cf=1.25, bf16).
+synthetic input, through the library's C ABI.  The headline workload is the
+64-expert layer (S=16384, d=2048, E=64, f=5120, top-2, cf=1.25, bf16).  The
+line also carries, under `configs`, the same measurement for every other
+layer configuration (the tiny fp32 layer, the 8-expert layer, the skewed
+16-expert layer with and without the capacity cap, and the 32-expert
+training step, forward + backward), and the decode shape and the PR-MoE
+forward of the 64-expert layer.
+
+Each configuration reports tokens/s, per-stage times, the expert GEMMs'
+TFLOP/s against the measured dense bf16 peak, the gate / dispatch / combine
+GB/s against the measured HBM copy bandwidth (in the loop, and with L2
+flushed before each launch), rows kept and tokens dropped, and -- in its
+`cpu_baseline` leg, where the float64 oracle is timed on the whole batch --
+how many tokens the oracle's own float64 routing sends elsewhere than the
+GPU (routing flips) and the largest top-k margin among them.
 
 Multi-GPU: the layer does not shard in this library, so N GPUs run N
 independent replicas (one process per GPU under torchrun); `value` is the
@@ -19,11 +33,11 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +48,10 @@ METRIC = "MoE-layer tokens/s (bf16 fwd/fwd+bwd); % of BF16 TC peak and HBM GB/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 GEMM_SOURCES = ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh", "kernels.h"]
+CONFIG_NAMES = ["tiny_fp32", "e8_bf16", "skew_e16_drop", "skew_e16_nodrop", "train_e32"]
+# a timed region this long under the power cap is held against the sustained
+# dense bf16 peak; shorter regions run at the burst clock
+SUSTAINED_REGION_S = 2.0
 
 
 def load_peaks():
@@ -53,9 +71,9 @@ def gemm_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, rows: int):
-    """DRAM bytes per GEMM launch from the committed ncu summary, scaled to
-    this launch's rows; None if the kernel source changed since."""
+def recorded_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary; None if the
+    kernel source changed since the capture."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as fh:
@@ -67,69 +85,112 @@ def recorded_traffic(workload: str, rows: int):
 
 
 def workload_desc(wl) -> str:
-    return (f"{wl.name}: MoE layer forward S={wl.num_tokens} d={wl.hidden_size} "
+    what = "forward+backward" if wl.backward else "forward"
+    return (f"{wl.name}: MoE layer {what} S={wl.num_tokens} d={wl.hidden_size} "
             f"E={wl.num_experts} f={wl.ffn_size} top-{wl.k} cf={wl.capacity_factor} "
-            f"min_cap={wl.min_capacity} drop={wl.drop_tokens} {wl.act} {wl.dtype}")
+            f"min_cap={wl.min_capacity} drop={wl.drop_tokens} {wl.act} {wl.dtype}"
+            + (f" skew={wl.skew}" if wl.skew else ""))
 
 
+def forward_launches(wl) -> int:
+    """Kernels one forward pass launches: the bf16 gate (fused gate kernel,
+    slot scan, slot assignment) or the fp32 gate (router GEMM, top-k, scan,
+    assignment), dispatch, the two expert GEMMs and the combine."""
+    return (3 if wl.dtype == "bf16" else 4) + 1 + 2 + 1
+
+
+# ------------------------------------------------------------------ clocks
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of one GPU, polled from a
+    background thread while the timed region runs (read-only NVML queries;
+    nvidia-smi at its fastest interval when NVML is not importable)."""
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
+
+    def __init__(self, device_index: int, interval_s: float = 0.0005):
+        self.index = device_index
+        self.interval = interval_s
+        self.rows = []
+        self.stop_evt = threading.Event()
+        self.thread = None
+        self.handle = None
+        self.nvml = None
+        self.source = "none"
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.handle = self._handle(pynvml)
+            self.sm_max = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
+            self.source = "nvml"
+        except Exception:
+            self.nvml = None
+
+    def _handle(self, pynvml):
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(self.index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            return pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return pynvml.nvmlDeviceGetHandleByIndex(self.index)
+
+    def _reasons(self):
+        try:
+            return self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
+        except Exception:
+            return self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
+
+    def _poll(self):
+        n = self.nvml
+        while not self.stop_evt.is_set():
+            try:
+                sm = float(n.nvmlDeviceGetClockInfo(self.handle, n.NVML_CLOCK_SM))
+                pw = n.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+                self.rows.append((sm, pw, int(self._reasons())))
+            except Exception:
+                pass
+            time.sleep(self.interval)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-            return
-        t0 = time.time()
-        while time.time() - t0 < 3.0:      # let nvidia-smi start reporting
-            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
-                break
-            time.sleep(0.05)
+        self.rows = []
+        self.stop_evt.clear()
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        rows = rows[1:] if len(rows) > 1 else rows   # first sample predates the load
-        os.unlink(self.path)
+        if self.thread is None:
+            return self._smi_once()
+        self.stop_evt.set()
+        self.thread.join()
+        self.thread = None
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": ["no samples"],
+                    "samples": 0, "source": self.source}
+        reasons = sorted({name for _, _, bits in rows for name, b in self.REASONS if bits & b})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_min_mhz": min(r[0] for r in rows),
+                "sm_max_mhz": self.sm_max, "power_w_max": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "source": self.source}
 
-        def num(v):
-            try:
-                return float(v)
-            except ValueError:
-                return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(rows)}
+    def _smi_once(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=10).stdout.strip().split(",")
+            v = [s.strip() for s in out]
+            names = [n for n, _ in self.REASONS]
+            return {"sm_mhz": float(v[0]), "sm_max_mhz": float(v[1]), "power_w_max": float(v[2]),
+                    "reasons": [names[i] for i in range(4) if v[3 + i] == "Active"],
+                    "samples": 1, "source": "nvidia-smi after the region"}
+        except Exception:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"],
+                    "samples": 0, "source": "none"}
 
 
 # ------------------------------------------------------------- replica timing
@@ -151,6 +212,168 @@ def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms: float) ->
     return world * tokens_per_step * steps / (ms * 1e-3)
 
 
+# ------------------------------------------------------------------ one layer
+STAGES = ("gate", "dispatch", "expert_ffn", "combine")
+
+
+class LayerRun:
+    """Device state of one workload (inputs, buffers, workspaces) and its
+    stage calls through the C ABI.  The forward runs the four stage entry
+    points, the kernels moe_forward launches in its order."""
+
+    def __init__(self, wl, dev):
+        import torch
+
+        from mixture_experts_layer_86_b300 import _native as N
+        from mixture_experts_layer_86_b300 import layer as L
+        from mixture_experts_layer_86_b300.inputs import make_inputs
+        self.N, self.torch = N, torch
+        self.wl = wl
+        self.cfg = N.config_from_workload(wl)
+        self.inp_cpu = make_inputs(wl)
+        self.d = self.inp_cpu.to(dev)
+        self.train = wl.backward
+        self.bufs = L.alloc_buffers(self.cfg, dev, training=self.train)
+        self.bufs["logits"] = None      # optional output of the gate; nothing downstream reads it
+        self.ws = L.alloc_workspace(self.cfg, dev)
+        self.y = torch.empty_like(self.d.x)
+        if self.train:
+            d = self.d
+            self.wsb = L.alloc_workspace(self.cfg, dev, for_backward=True)
+            self.grads = {"dx": torch.empty_like(d.x), "dw_gate": torch.empty_like(d.w_gate),
+                          "dw1": torch.empty_like(d.w1), "db1": torch.empty_like(d.b1),
+                          "dw2": torch.empty_like(d.w2), "db2": torch.empty_like(d.b2)}
+
+    def stage(self, name, st):
+        N, d, b, c = self.N, self.d, self.bufs, self.cfg
+        if name == "gate":
+            N.moe_gate_topk(c, d.x, d.w_gate, d.logit_bias, b["logits"], b["probs"], b["topk_idx"],
+                            b["topk_w"], b["slot"], b["routed_cnt"], b["kept_cnt"],
+                            b["expert_offsets"], b["row_src"], b["l_aux"], self.ws, st)
+        elif name == "dispatch":
+            N.moe_dispatch(c, d.x, b["topk_idx"], b["slot"], b["expert_offsets"], b["x_disp"], st)
+        elif name == "expert_ffn":
+            N.moe_expert_ffn(c, b["x_disp"], b["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
+                             b["h_pre"], b["h"], b["out_disp"], st)
+        elif name == "combine":
+            N.moe_combine(c, b["out_disp"], b["topk_idx"], b["slot"], b["expert_offsets"],
+                          b["topk_w"], self.y, st)
+        elif name == "backward":
+            g = self.grads
+            N.moe_backward(c, d.x, d.w_gate, d.w1, d.w2, b, d.dy, g["dx"], g["dw_gate"], g["dw1"],
+                           g["db1"], g["dw2"], g["db2"], self.wsb, st)
+
+    def step(self, st, ev=None, marks=()):
+        """One step; ev[i] is recorded just before the i-th stage named in
+        `marks` ("end": after the last stage)."""
+        names = STAGES + (("backward",) if self.train else ())
+        j = 0
+        for name in names + ("end",):
+            if ev is not None and name in marks:
+                ev[j].record(st)
+                j += 1
+            if name != "end":
+                self.stage(name, st)
+
+    def rows(self) -> int:
+        return int(self.bufs["expert_offsets"][-1].item())
+
+
+def _events(torch, n_steps, n_ev):
+    return [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_steps)]
+
+
+def timed(torch, st, steps, body, barrier=None):
+    """Milliseconds of `steps` calls of body(i) between two events on st."""
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        body(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1)
+
+
+def stage_bytes(wl, R, with_probs=False):
+    """Algorithmic HBM bytes of the gate, dispatch and combine stages: each
+    input read once, each output written once."""
+    S, d, E, k = wl.num_tokens, wl.hidden_size, wl.num_experts, wl.k
+    eb = 2 if wl.dtype == "bf16" else 4
+    return {"gate": S * d * eb + E * d * eb + S * k * 12 + R * 4 + (S * E * 4 if with_probs else 0),
+            "dispatch": S * d * eb + R * d * eb + S * k * 8,
+            "combine": R * d * eb + S * d * eb + S * k * 12}
+
+
+def stage_breakdown(run, st, steps, peaks):
+    """Per-stage times from a loop with an event at every stage boundary (a
+    separate loop from the headline one, so its events do not perturb it)."""
+    torch = run.torch
+    names = STAGES + (("backward",) if run.train else ())
+    evs = _events(torch, steps, len(names) + 1)
+    timed(torch, st, steps, lambda i: run.step(st, evs[i], marks=names + ("end",)))
+    ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
+    R = run.rows()
+    wl = run.wl
+    byt = stage_bytes(wl, R, with_probs=run.train)
+    out = {}
+    for n in names:
+        ent = {"ms": ms[n]}
+        if n in byt:
+            gbs = byt[n] / (ms[n] * 1e-3) / 1e9
+            ent.update({"bytes": byt[n], "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
+        out[n] = ent
+    ffn_flops = 4.0 * R * wl.hidden_size * wl.ffn_size
+    out["expert_ffn"]["TFLOP/s"] = ffn_flops / (ms["expert_ffn"] * 1e-3) / 1e12
+    if wl.dtype == "bf16":
+        out["expert_ffn"]["frac_bf16_burst"] = out["expert_ffn"]["TFLOP/s"] / peaks["bf16_tflops"]
+    return out
+
+
+def stages_cold_l2(run, st, peaks, reps=10):
+    """Gate, dispatch and combine launched alone with L2 flushed before each
+    launch (a 512 MB write): their HBM bandwidth without help from data
+    that an earlier stage left in the 126 MB L2."""
+    torch = run.torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=run.d.x.device)
+    R = run.rows()
+    byt = stage_bytes(run.wl, R, with_probs=run.train)
+    out = {}
+    for n in ("gate", "dispatch", "combine"):
+        t = []
+        for i in range(reps):
+            flush.fill_(i & 0xff)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            run.stage(n, st)
+            e1.record(st)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        ms = statistics.median(t)
+        gbs = byt[n] / (ms * 1e-3) / 1e9
+        out[n] = {"ms": ms, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
+    del flush
+    return out
+
+
+def routing_stats(run):
+    import numpy as np
+    b = run.bufs
+    slot = b["slot"].cpu().numpy()
+    routed = b["routed_cnt"].cpu().numpy()
+    kept = b["kept_cnt"].cpu().numpy()
+    S, k = run.wl.num_tokens, run.wl.k
+    R = int(kept.sum())
+    return {"rows_kept": R, "dropped_choices": int(S * k - R),
+            "fully_dropped_tokens": int(np.count_nonzero((slot < 0).all(axis=1))),
+            "routed_max": int(routed.max()), "routed_min": int(routed.min()),
+            "experts_used": int(np.count_nonzero(kept))}
+
+
 # --------------------------------------------------------------------- GPU arm
 def run_gpu(args):
     import torch
@@ -158,7 +381,7 @@ def run_gpu(args):
 
     from mixture_experts_layer_86_b300 import _native as N
     from mixture_experts_layer_86_b300 import layer as L
-    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -175,83 +398,43 @@ def run_gpu(args):
     def max_over_ranks(v: float) -> float:
         return reduce_max(v, world, dev)
 
+    peaks, peak_src = load_peaks()
     wl = WORKLOADS[args.workload]
-    cfg = N.config_from_workload(wl)
-    inp_cpu = make_inputs(wl)
-    d = inp_cpu.to(dev)
-    bufs = L.alloc_buffers(cfg, dev)
-    bufs["logits"] = None      # optional output of the gate; nothing downstream reads it
-    ws = L.alloc_workspace(cfg, dev)
-    y = torch.empty_like(d.x)
+    run = LayerRun(wl, dev)
+    cfg, d = run.cfg, run.d
     st = torch.cuda.current_stream()
-    S, dm, f, E, k = wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k
+    S, dm, f, E = wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts
     eb = 2 if wl.dtype == "bf16" else 4
 
-    n_ev = 5
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for _ in range(max(args.warmup, 3)):
+        run.step(st)
+    torch.cuda.synchronize()
+    R = run.rows()
 
-    def step(ev=None):
-        # one forward pass through the four stage entry points (the kernels
-        # moe_forward launches, in its order), with events between stages
-        if ev is not None:
-            ev[0].record(st)
-        N.moe_gate_topk(cfg, d.x, d.w_gate, d.logit_bias, bufs["logits"], None, bufs["topk_idx"],
-                        bufs["topk_w"], bufs["slot"], bufs["routed_cnt"], bufs["kept_cnt"],
-                        bufs["expert_offsets"], bufs["row_src"], bufs["l_aux"], ws, st)
-        if ev is not None:
-            ev[1].record(st)
-        N.moe_dispatch(cfg, d.x, bufs["topk_idx"], bufs["slot"], bufs["expert_offsets"],
-                       bufs["x_disp"], st)
-        if ev is not None:
-            ev[2].record(st)
-        N.moe_expert_ffn(cfg, bufs["x_disp"], bufs["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
-                         None, bufs["h"], bufs["out_disp"], st)
-        if ev is not None:
-            ev[3].record(st)
-        N.moe_combine(cfg, bufs["out_disp"], bufs["topk_idx"], bufs["slot"],
-                      bufs["expert_offsets"], bufs["topk_w"], y, st)
-        if ev is not None:
-            ev[4].record(st)
-
+    # ---- value: K forward steps, inputs resident in HBM.  The only events
+    # inside are the two around the expert FFN (its two GEMM launches), which
+    # give the dominant kernel's launch time for the roofline.
+    ffn_ev = _events(torch, args.steps, 2)
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    R = int(bufs["expert_offsets"][-1].item())
-
-    # ---- value: K forward steps, inputs resident in HBM; the per-stage
-    # times (and the expert GEMM's launch time for the roofline) come from
-    # the events inside this same timed region
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(args.steps):
-        step(evs[i])
-    e1.record(st)
-    torch.cuda.synchronize()
-    barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1))
-    stage_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in evs)
-                for j, name in enumerate(["gate", "dispatch", "expert_ffn", "combine"])}
-
-    # ---- cross-check: the same K steps through the single moe_forward call
-    e0.record(st)
-    for _ in range(args.steps):
-        N.moe_forward(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, y, bufs, ws, st)
-    e1.record(st)
-    torch.cuda.synchronize()
-    fwd_call_ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = timed(torch, st, args.steps,
+               lambda i: run.step(st, ffn_ev[i], marks=("expert_ffn", "combine")), barrier)
     clocks = sampler.stop()
-    train = train_step(args, dev, barrier, max_over_ranks, world)
-    decode = decode_step(args, dev, max_over_ranks, world)
-    residual = residual_step(args, dev, d, cfg, wl, max_over_ranks, world)
+    ms = max_over_ranks(ms)
+    ffn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ffn_ev)
+
+    # ---- the same K steps through the single moe_forward call
+    fwd_call_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
+        cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, run.bufs, run.ws, st)))
+    stages = stage_breakdown(run, st, args.steps, peaks)
+    cold = stages_cold_l2(run, st, peaks)
+    rstats = routing_stats(run)
 
     # ---- e2e: host buffers, copies inside the timed region.  Each step
     # copies its batch host -> device, runs moe_forward and copies y, l_aux
     # and the expert counts back; HostPipeline overlaps the copies of
     # neighbouring steps with the forward (two slots, three streams).
+    inp_cpu = run.inp_cpu
     x_host = [inp_cpu.x.pin_memory(), inp_cpu.x.clone().pin_memory()]
     y_host = [torch.empty_like(inp_cpu.x).pin_memory() for _ in range(2)]
     laux_host = [torch.empty((1,), dtype=torch.float32).pin_memory() for _ in range(2)]
@@ -266,6 +449,7 @@ def run_gpu(args):
     pipe.synchronize()
     torch.cuda.synchronize()
     barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(pipe.s_in)            # before the first copy in
     e2e_run(args.steps)
     e1.record(pipe.s_out)           # after the last copy out
@@ -274,38 +458,49 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
     barrier()
     # the last step's result really is on the host
-    assert torch.equal(y_host[(args.steps - 1) % 2], y.cpu()), "e2e result differs"
+    assert torch.equal(y_host[(args.steps - 1) % 2], run.y.cpu()), "e2e result differs"
+    del pipe
+
+    decode = decode_step(args, dev, max_over_ranks, world, peaks)
+    residual = residual_step(args, dev, run, max_over_ranks, world)
+    gpu_idx = run.bufs["topk_idx"].cpu().numpy()
+    del run
+    torch.cuda.empty_cache()
+    configs = {}
+    if not args.no_configs:
+        for name in CONFIG_NAMES:
+            configs[name] = config_line(WORKLOADS[name], args, dev, st, peaks, max_over_ranks,
+                                        world, barrier, rank == 0 and not args.no_cpu)
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peaks, peak_src = load_peaks()
-    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    flops_launch = 2.0 * R * dm * f           # one of the two equal expert GEMMs
-    gemm_launch_ms = stage_ms["expert_ffn"] / 2.0
+    # ---- roofline of the dominant kernel, the expert GEMM: 2 R d f FLOP per
+    # launch over the average of its two launches (W1 and W2, equal FLOPs)
+    flops_launch = 2.0 * R * dm * f
+    gemm_launch_ms = ffn_ms / 2.0
     achieved = flops_launch / (gemm_launch_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(wl.name, R)
-    hbm_peak = peaks["hbm_gbs"]
-
-    def gbs(nbytes, ms_):
-        return nbytes / (ms_ * 1e-3) / 1e9
-
-    gate_bytes = S * dm * eb + E * dm * eb + S * k * 12 + R * 4
-    disp_bytes = S * dm * eb + R * dm * eb + S * k * 8
-    comb_bytes = R * dm * eb + S * dm * eb + S * k * 12
-    stages = {
-        "gate": {"ms": stage_ms["gate"], "GB/s": gbs(gate_bytes, stage_ms["gate"]),
-                 "frac_hbm": gbs(gate_bytes, stage_ms["gate"]) / hbm_peak},
-        "dispatch": {"ms": stage_ms["dispatch"], "GB/s": gbs(disp_bytes, stage_ms["dispatch"]),
-                     "frac_hbm": gbs(disp_bytes, stage_ms["dispatch"]) / hbm_peak},
-        "expert_ffn": {"ms": stage_ms["expert_ffn"],
-                       "TFLOP/s": 2 * flops_launch / (stage_ms["expert_ffn"] * 1e-3) / 1e12},
-        "combine": {"ms": stage_ms["combine"], "GB/s": gbs(comb_bytes, stage_ms["combine"]),
-                    "frac_hbm": gbs(comb_bytes, stage_ms["combine"]) / hbm_peak},
-    }
-    launches_per_step = 7  # gate, scan, assign, dispatch, 2 expert GEMMs, combine
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
+    long_capped = ms * 1e-3 >= SUSTAINED_REGION_S and "sw_power_cap" in clocks.get("reasons", [])
+    peak = sustained if long_capped else burst
+    roofline = {
+        "bound": "tensor", "kernel": "tc_gemm_pair_kernel (expert GEMM; mean of its two launches)",
+        "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+        "frac_burst": achieved / burst, "frac_sustained": achieved / sustained,
+        "peak_source": (f"{peak_src} dense bf16 "
+                        + ("sustained (timed region >= 2 s under the power cap)" if long_capped
+                           else f"burst (timed region {ms:.1f} ms)")
+                        + f"; burst {burst}, sustained {sustained} TFLOP/s"),
+        "flops_per_launch": flops_launch, "launch_ms": gemm_launch_ms,
+        "traffic": recorded_traffic(wl.name),
+        "traffic_note": "DRAM bytes per launch from the committed ncu capture "
+                        "(profiles/roofline_traffic.json) while the GEMM sources are unchanged, "
+                        "else null"}
+    cpu = cpu_baseline(wl, inp_cpu, gpu_idx) if not args.no_cpu else None
     line = {
         "metric": METRIC,
         "value": job_tokens_per_s(world, S, args.steps, ms),
@@ -319,27 +514,15 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
-        "config": {"workload": workload_desc(wl), "rows_kept": R,
-                   "capacity": N.moe_capacity(cfg),
+        "config": {"workload": workload_desc(wl), "capacity": N.moe_capacity(cfg),
+                   **rstats,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "no flush: each step streams 2.7 GB of expert weights, 21x the 126 MB L2"},
-        "roofline": {"bound": "tensor", "kernel": "tc_gemm_pair_kernel (expert GEMM, one launch)",
-                     "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": achieved / peak_sus,
-                     "frac_burst": achieved / peaks["bf16_tflops"],
-                     "peak_source": f"{peak_src} dense bf16, sustained (the GEMM runs inside "
-                                    f"a {args.steps}-step loop under the power cap); burst "
-                                    f"{peaks['bf16_tflops']} TFLOP/s",
-                     "flops_per_launch": flops_launch,
-                     "launch_ms": gemm_launch_ms,
-                     "traffic": traffic,
-                     "traffic_note": "DRAM bytes per launch from the committed ncu capture "
-                                     "(profiles/roofline_traffic.json) while the GEMM sources "
-                                     "are unchanged, else null"},
+                   "l2": "no flush in the timed loop: each step streams 2.7 GB of expert "
+                         "weights, 21x the 126 MB L2 (stages_cold_l2: gate, dispatch and "
+                         "combine alone after a 512 MB flush)"},
+        "roofline": roofline,
         "stages": stages,
-        "train_step": train,
-        "decode_step": decode,
-        "residual_step": residual,
+        "stages_cold_l2": cold,
         "e2e": {"value": job_tokens_per_s(world, S, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": S * dm * eb,
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
@@ -347,85 +530,60 @@ def run_gpu(args):
                 "timing": "CUDA events: before the first host-to-device copy, after the last "
                           "device-to-host copy"},
         "moe_forward_ms_per_step": fwd_call_ms / args.steps,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": forward_launches(wl) * args.steps,
         "clocks": clocks,
-        "cpu_baseline": cpu_baseline(wl, inp_cpu, args),
+        "configs": configs,
+        "decode_step": decode,
+        "residual_step": residual,
+        "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def train_step(args, dev, barrier, max_over_ranks, world):
-    """Forward + backward of the 32-expert training layer."""
+def config_line(wl, args, dev, st, peaks, max_over_ranks, world, barrier, with_cpu):
+    """One layer configuration, measured like the headline workload."""
     import torch
-
-    from mixture_experts_layer_86_b300 import _native as N
-    from mixture_experts_layer_86_b300 import layer as L
-    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
-
-    wl = WORKLOADS["train_e32"]
-    cfg = N.config_from_workload(wl)
-    d = make_inputs(wl).to(dev)
-    bufs = L.alloc_buffers(cfg, dev, training=True)
-    ws = L.alloc_workspace(cfg, dev)
-    wsb = L.alloc_workspace(cfg, dev, for_backward=True)
-    y = torch.empty_like(d.x)
-    grads = {"dx": torch.empty_like(d.x), "dw_gate": torch.empty_like(d.w_gate),
-             "dw1": torch.empty_like(d.w1), "db1": torch.empty_like(d.b1),
-             "dw2": torch.empty_like(d.w2), "db2": torch.empty_like(d.b2)}
-    st = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    fw, bw = [], []
-
-    def step(timed):
-        if timed:
-            ev[0].record(st)
-        N.moe_forward(cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, y, bufs, ws, st)
-        if timed:
-            ev[1].record(st)
-        N.moe_backward(cfg, d.x, d.w_gate, d.w1, d.w2, bufs, d.dy, grads["dx"], grads["dw_gate"],
-                       grads["dw1"], grads["db1"], grads["dw2"], grads["db2"], wsb, st)
-        if timed:
-            ev[2].record(st)
-
+    run = LayerRun(wl, dev)
     for _ in range(max(args.warmup, 3)):
-        step(False)
+        run.step(st)
     torch.cuda.synchronize()
-    R = int(bufs["expert_offsets"][-1].item())
-    steps = max(1, min(args.steps, 100))
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(steps):
-        step(False)
-    e1.record(st)
-    torch.cuda.synchronize()
-    barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1))
-    for _ in range(5):
-        step(True)
-        torch.cuda.synchronize()
-        fw.append(ev[0].elapsed_time(ev[1]))
-        bw.append(ev[1].elapsed_time(ev[2]))
-    flops = 12.0 * R * wl.hidden_size * wl.ffn_size   # expert GEMMs: 4 fwd + 8 bwd
-    return {"workload": workload_desc(wl).replace("forward", "forward+backward"),
-            "value": job_tokens_per_s(world, wl.num_tokens, steps, ms), "unit": "tokens/s",
-            "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
-            "fwd_ms": statistics.median(fw), "bwd_ms": statistics.median(bw),
-            "expert_gemm_TFLOP/s": flops / (ms / steps * 1e-3) / 1e12}
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    ms = max_over_ranks(timed(torch, st, args.steps, lambda i: run.step(st), barrier))
+    clocks = sampler.stop()
+    stages = stage_breakdown(run, st, args.steps, peaks)
+    R = run.rows()
+    out = {"workload": workload_desc(wl),
+           "value": job_tokens_per_s(world, wl.num_tokens, args.steps, ms), "unit": "tokens/s",
+           "ms_per_step": ms / args.steps, "steps": args.steps, **routing_stats(run),
+           "stages": stages, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "reasons", "samples")}}
+    gemm_flops = (12.0 if wl.backward else 4.0) * R * wl.hidden_size * wl.ffn_size
+    step_tflops = gemm_flops / (ms / args.steps * 1e-3) / 1e12
+    out["expert_gemm_TFLOP/s_over_step"] = step_tflops
+    if wl.dtype == "bf16":
+        out["expert_gemm_frac_bf16_burst_over_step"] = step_tflops / peaks["bf16_tflops"]
+        out["stages_cold_l2"] = stages_cold_l2(run, st, peaks)
+    if wl.backward:
+        bwd_flops = 8.0 * R * wl.hidden_size * wl.ffn_size
+        out["backward_TFLOP/s"] = bwd_flops / (stages["backward"]["ms"] * 1e-3) / 1e12
+    if with_cpu:
+        out["cpu_baseline"] = cpu_baseline(wl, run.inp_cpu, run.bufs["topk_idx"].cpu().numpy())
+    del run
+    return out
 
 
-def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
+def residual_step(args, dev, run, max_over_ranks, world):
     """PR-MoE forward (moe_forward_residual: the layer plus a dense MLP of
-    one expert's shape on every token) on the same workload."""
+    one expert's shape on every token) on the headline workload."""
     import torch
 
     from mixture_experts_layer_86_b300 import _native as N
     from mixture_experts_layer_86_b300 import layer as L
     from mixture_experts_layer_86_b300.inputs import make_residual_mix, make_residual_weights
 
+    wl, cfg, d = run.wl, run.cfg, run.d
     rw = [t.to(dev) for t in make_residual_weights(wl)]
     mix_w, mix_b = [t.to(dev) for t in make_residual_mix(wl)]
     bufs = L.alloc_buffers(cfg, dev)
@@ -456,13 +614,7 @@ def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
     total = {False: 0.0, True: 0.0}
     for b in range(blocks):
         for learned in ((False, True) if b % 2 == 0 else (True, False)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            for _ in range(per_block):
-                step(learned)
-            e1.record(st)
-            torch.cuda.synchronize()
-            total[learned] += e0.elapsed_time(e1)
+            total[learned] += timed(torch, st, per_block, lambda i: step(learned))
     ms = max_over_ranks(total[False])
     ms_mix = max_over_ranks(total[True])
     R = int(bufs["expert_offsets"][-1].item())
@@ -475,92 +627,77 @@ def residual_step(args, dev, d, cfg, wl, max_over_ranks, world):
                             "unit": "tokens/s", "ms_per_step": ms_mix / steps}}
 
 
-def decode_step(args, dev, max_over_ranks, world):
+def decode_step(args, dev, max_over_ranks, world, peaks):
     """Inference shape: one decode step of 256 sequences through the 64-expert
     layer.  Each expert sees a handful of tokens, so the expert GEMMs stream
     the routed experts' weights: their roofline is HBM bandwidth."""
     import torch
 
-    from mixture_experts_layer_86_b300 import _native as N
-    from mixture_experts_layer_86_b300 import layer as L
-    from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
+    from mixture_experts_layer_86_b300.inputs import WORKLOADS
 
     wl = WORKLOADS["decode_e64"]
-    cfg = N.config_from_workload(wl)
-    d = make_inputs(wl).to(dev)
-    bufs = L.alloc_buffers(cfg, dev)
-    bufs["logits"] = None
-    ws = L.alloc_workspace(cfg, dev)
-    y = torch.empty_like(d.x)
+    run = LayerRun(wl, dev)
     st = torch.cuda.current_stream()
     steps = max(1, min(args.steps, 200))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-
-    def step(e=None):
-        if e is not None:
-            e[0].record(st)
-        N.moe_gate_topk(cfg, d.x, d.w_gate, d.logit_bias, bufs["logits"], None, bufs["topk_idx"],
-                        bufs["topk_w"], bufs["slot"], bufs["routed_cnt"], bufs["kept_cnt"],
-                        bufs["expert_offsets"], bufs["row_src"], bufs["l_aux"], ws, st)
-        N.moe_dispatch(cfg, d.x, bufs["topk_idx"], bufs["slot"], bufs["expert_offsets"],
-                       bufs["x_disp"], st)
-        if e is not None:
-            e[1].record(st)
-        N.moe_expert_ffn(cfg, bufs["x_disp"], bufs["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
-                         None, bufs["h"], bufs["out_disp"], st)
-        if e is not None:
-            e[2].record(st)
-        N.moe_combine(cfg, bufs["out_disp"], bufs["topk_idx"], bufs["slot"],
-                      bufs["expert_offsets"], bufs["topk_w"], y, st)
-
     for _ in range(max(args.warmup, 3)):
-        step()
+        run.step(st)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(steps):
-        step(ev[i])
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1))
-    ffn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    kept = bufs["kept_cnt"].cpu()
-    R = int(kept.sum())
+    ev = _events(torch, steps, 2)
+    ms = max_over_ranks(timed(torch, st, steps,
+                              lambda i: run.step(st, ev[i], marks=("expert_ffn", "combine"))))
+    ffn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    rs = routing_stats(run)
+    R, used = rs["rows_kept"], rs["experts_used"]
     dm, f = wl.hidden_size, wl.ffn_size
-    used = int((kept > 0).sum())
     # algorithmic bytes of the two expert GEMMs: the weights (and biases) of
     # every expert with a kept token, x_disp in, h out and back in, out_disp out
     ffn_bytes = used * (2 * f * dm + f + dm) * 2 + R * (2 * dm + 2 * f) * 2
-    peaks, _ = load_peaks()
     gbs = ffn_bytes / (ffn_ms * 1e-3) / 1e9
     return {"workload": workload_desc(wl), "value": job_tokens_per_s(world, wl.num_tokens, steps, ms),
-            "unit": "tokens/s", "ms_per_step": ms / steps, "steps": steps, "rows_kept": R,
-            "experts_used": used,
+            "unit": "tokens/s", "ms_per_step": ms / steps, "steps": steps, **rs,
             "expert_ffn": {"ms": ffn_ms, "bytes": ffn_bytes, "GB/s": gbs, "bound": "hbm",
                            "frac_hbm": gbs / peaks["hbm_gbs"]}}
 
 
 # ------------------------------------------------------------------- CPU oracle
-def _oracle_forward_tokens(wl, inp_cpu, n):
+def _f32_numpy(t):
     import torch
+    return t.to(torch.float32).numpy()
+
+
+def _oracle_config(wl, n):
     from oracle import moe_oracle as O
-    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
-    cfg = O.LayerConfig(n, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k,
-                        wl.capacity_factor, wl.min_capacity, wl.drop_tokens, wl.act)
-    lb = None if inp_cpu.logit_bias is None else f64(inp_cpu.logit_bias)
-    return O.forward(cfg, f64(inp_cpu.x[:n]), f64(inp_cpu.w_gate), inp_cpu.w1_f64,
-                     inp_cpu.b1_f64, inp_cpu.w2_f64, inp_cpu.b2_f64, logit_bias=lb)
+    return O.LayerConfig(n, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k,
+                         wl.capacity_factor, wl.min_capacity, wl.drop_tokens, wl.act,
+                         wl.aux_loss_weight, wl.gate_temperature, wl.aux_loss_type)
 
 
-def _prepare_oracle_weights(inp_cpu):
-    # exact float32 copies of the bf16 weights; the oracle widens each
-    # expert's slice to float64 itself
+def _oracle_step(wl, inp_cpu, n):
+    """The oracle's forward (and, for a training workload, backward) on the
+    first n tokens; the weights are passed as exact float32 copies of the
+    bf16 values and the oracle widens each expert's slice to float64."""
+    import numpy as np
     import torch
-    if not hasattr(inp_cpu, "w1_f64"):
-        inp_cpu.w1_f64 = inp_cpu.w1.to(torch.float32).numpy()
-        inp_cpu.b1_f64 = inp_cpu.b1.to(torch.float32).numpy()
-        inp_cpu.w2_f64 = inp_cpu.w2.to(torch.float32).numpy()
-        inp_cpu.b2_f64 = inp_cpu.b2.to(torch.float32).numpy()
+
+    from oracle import moe_oracle as O
+    x = inp_cpu.x[:n].to(torch.float64).numpy()
+    w = getattr(inp_cpu, "_f32", None)
+    if w is None:
+        w = [_f32_numpy(t) for t in (inp_cpu.w_gate, inp_cpu.w1, inp_cpu.b1, inp_cpu.w2,
+                                     inp_cpu.b2)]
+        inp_cpu._f32 = w
+    wg, w1, b1, w2, b2 = w
+    lb = inp_cpu.logit_bias
+    if lb is not None:
+        lb = lb.to(torch.float64).numpy()
+        if lb.ndim == 2:
+            lb = lb[:n]
+    cfg = _oracle_config(wl, n)
+    fwd = O.forward(cfg, x, wg, w1, b1, w2, b2, logit_bias=lb)
+    if wl.backward:
+        dy = inp_cpu.dy[:n].to(torch.float64).numpy()
+        O.backward(cfg, fwd, x, wg, w1, w2, dy)
+    return fwd, np.asarray(fwd["logits"])
 
 
 def _blas_threads() -> int:
@@ -572,21 +709,31 @@ def _blas_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, inp_cpu, args, budget_s: float = 12.0):
-    """The oracle, as it stands, on the first n tokens of the same workload;
-    n grows until one run takes at least budget_s (or covers the batch)."""
-    _prepare_oracle_weights(inp_cpu)
-    n = 64
-    while True:
-        t0 = time.perf_counter()
-        _oracle_forward_tokens(wl, inp_cpu, n)
-        dt = time.perf_counter() - t0
-        if dt >= budget_s or n >= wl.num_tokens:
-            break
-        n = min(wl.num_tokens, int(n * max(1.5, min(8.0, 1.2 * budget_s / max(dt, 1e-3)))))
-    return {"value": n / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"float64 oracle forward on the first {n} of {wl.num_tokens} tokens "
-                      f"(same layer, capacity recomputed for the sample), {dt:.1f} s"}
+def cpu_baseline(wl, inp_cpu, gpu_idx=None):
+    """The oracle, as it stands, timed on the whole batch of the workload (a
+    forward, or forward + backward for the training step).  Its own float64
+    routing of that batch is compared with the GPU's: tokens routed
+    differently are routing flips, reported with the largest top-k margin
+    (float64 logits) among them."""
+    import numpy as np
+    S = wl.num_tokens
+    t0 = time.perf_counter()
+    fwd, logits = _oracle_step(wl, inp_cpu, S)
+    dt = time.perf_counter() - t0
+    out = {"value": S / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+           "sample": f"float64 oracle {'forward+backward' if wl.backward else 'forward'} on the "
+                     f"whole batch of {S} tokens (one run, {dt:.1f} s, weight widening included)"}
+    if gpu_idx is not None:
+        own = fwd["routing"].idx
+        flips = np.nonzero(np.any(own != gpu_idx, axis=1))[0]
+        srt = -np.sort(-logits, axis=1)
+        k = wl.k
+        margin = srt[:, k - 1] - srt[:, k] if logits.shape[1] > k else np.full(S, np.inf)
+        if k == 2:
+            margin = np.minimum(margin, srt[:, 0] - srt[:, 1])
+        out["routing_flips"] = int(len(flips))
+        out["flip_max_margin"] = float(margin[flips].max()) if len(flips) else None
+    return out
 
 
 def run_reference(args):
@@ -596,22 +743,33 @@ def run_reference(args):
     from mixture_experts_layer_86_b300.inputs import WORKLOADS, make_inputs
     wl = WORKLOADS[args.workload]
     inp_cpu = make_inputs(wl)
-    _prepare_oracle_weights(inp_cpu)
+    # the oracle's time grows as a + b n with the batch n (a: widening every
+    # used expert's weights to float64 once per call); two batch sizes, both
+    # large enough that every expert gets tokens, give a and b
+    n1 = min(wl.num_tokens, 4 * wl.num_experts)
+    n2 = min(wl.num_tokens, 3 * n1)
     t0 = time.perf_counter()
-    _oracle_forward_tokens(wl, inp_cpu, 32)
-    per_tok = (time.perf_counter() - t0) / 32
+    _oracle_step(wl, inp_cpu, n1)
+    t1 = time.perf_counter()
+    _oracle_step(wl, inp_cpu, n2)
+    t2 = time.perf_counter()
+    per_tok = max((t2 - t1) - (t1 - t0), 1e-9) / max(n2 - n1, 1)
+    fixed = max(0.0, (t1 - t0) - per_tok * n1)
     total_budget = 150.0
     per_step = total_budget / max(1, args.steps + args.warmup)
-    n = int(min(wl.num_tokens, max(8, per_step / max(per_tok, 1e-9))))
+    n = int(min(wl.num_tokens, max(8, (per_step - fixed) / per_tok)))
     for _ in range(args.warmup):
-        _oracle_forward_tokens(wl, inp_cpu, n)
+        _oracle_step(wl, inp_cpu, n)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_forward_tokens(wl, inp_cpu, n)
+        _oracle_step(wl, inp_cpu, n)
     dt = time.perf_counter() - t0
     v = n * args.steps / dt
     sample = (f"float64 oracle forward on the first {n} of {wl.num_tokens} tokens per step "
-              f"(same layer, capacity recomputed for the sample)")
+              f"(same layer, capacity recomputed for the sample); each call also pays a fixed "
+              f"{fixed:.2f} s of weight widening, so the whole batch would take about "
+              f"{fixed + per_tok * wl.num_tokens:.1f} s ({1.0 / per_tok:.0f} tokens/s after the "
+              f"fixed cost)")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
@@ -619,7 +777,9 @@ def run_reference(args):
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(wl), "tokens_per_step": n},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": _blas_threads(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "tokens_per_s_after_fixed_cost": 1.0 / per_tok,
+                             "fixed_cost_s_per_call": fixed},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -628,10 +788,13 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="e64_bf16")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the headline workload, the decode and PR-MoE legs")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baselines")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

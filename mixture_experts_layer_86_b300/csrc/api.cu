@@ -3,8 +3,6 @@
 // The entry points and their contracts are documented in moe_b300.h.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 #include "moe_b300.h"
@@ -15,8 +13,6 @@ __device__ unsigned int g_device_error = 0;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 float inv_temperature(const moe_config *c) {
@@ -24,17 +20,16 @@ float inv_temperature(const moe_config *c) {
 }
 
 unsigned int *device_error_ptr() {
-  static unsigned int *ptrs[kMaxDevices] = {nullptr};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned int *>(p);
-  }
-  return ptrs[dev];
+  static PerDevice<unsigned int *> ptrs;
+  unsigned int *p = nullptr;
+  if (ptrs.get(&p, [](unsigned int *&v) {
+        void *a = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&a, g_device_error);
+        v = static_cast<unsigned int *>(a);
+        return e;
+      }) != cudaSuccess)
+    return nullptr;
+  return p;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -224,16 +219,17 @@ moe_status dense_mlp(const moe_config *c, const void *x, const void *rw1, const 
 }  // namespace
 
 int num_sms() {
-  static int cached[kMaxDevices] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
+  static PerDevice<int> cached;
+  int n = 0;
+  if (cached.get(&n, [](int &v) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess && v <= 0) e = cudaErrorInvalidValue;
+        return e;
+      }) != cudaSuccess)
+    return 148;
+  return n;
 }
 
 }  // namespace moe

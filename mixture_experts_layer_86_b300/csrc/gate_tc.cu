@@ -32,6 +32,8 @@ namespace moe {
 namespace {
 
 constexpr int GBM = 128, GBK = 64, kMaxGateStages = 8;
+// the routing scan reads the per-CTA histogram rows this kernel writes
+static_assert(GBM == kRouteTokensPerCta, "gate tile and routing CTA must cover the same tokens");
 constexpr int kGateThreads = 512;  // 16 warps
 constexpr uint32_t kGateABytes = GBM * GBK * 2;  // 16 KB
 constexpr uint64_t kGateWaitNs = 2000000000ull;
@@ -377,13 +379,13 @@ cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st) {
   if (ring < tile_bytes) ring = tile_bytes;
   const size_t smem = fixed + ring;
   if (smem > kSmemLimit) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemLimit));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<int> smem_raised;
+  int unused = 0;
+  if (const cudaError_t e = smem_raised.get(&unused, [&](int &) {
+        return cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kSmemLimit));
+      }); e != cudaSuccess)
+    return e;
   const uint32_t idesc = ptx::idesc_bf16(GBM, E_pad, 0, 0);
   return launch_k(gate_tc_kernel, unsigned(nblk), kGateThreads, smem, st, tx, tw, a.S, a.d, a.E,
                   E_pad, a.k, idesc, cols, nstages, uint32_t(ring), a.logit_bias, a.bias_ld,

@@ -52,7 +52,6 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxGroups = kMaxExperts;
-constexpr int kMaxDevices = 64;
 // swapped-operand grouped GEMM: BM output features x up to BN tokens
 constexpr int kFeat = BM, kTok = BN;
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 tokens x 32 bf16 features
@@ -977,14 +976,13 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
   if (!make_map(&ta, g.A, uint64_t(g.M), uint64_t(g.rows_alloc), 64, BK) ||
       !make_map(&tb, g.B, uint64_t(g.N), uint64_t(g.rows_alloc), 64, BK))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kWgSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<int> smem_raised;
+  int unused = 0;
+  if (const cudaError_t e = smem_raised.get(&unused, [](int &) {
+        return cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kWgSmemBytes));
+      }); e != cudaSuccess)
+    return e;
   const int tiles = g.G * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_k(tc_wgrad_kernel, grid, kWgThreads, kWgSmemBytes, st, ta, tb, g.offsets, g.G, g.M,
@@ -1022,39 +1020,39 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     lc.stream = st;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    // persistent grid: as many pairs as can be resident at once
-    static int pairs[kMaxDevices][2] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (pairs[dev][which] == 0) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kPairSmemBytes));
-      if (e != cudaSuccess) return e;
+    // persistent grid: as many pairs as can be resident at once (the
+    // shared-memory limit is raised and the occupancy asked once per device)
+    static PerDevice<int> resident_pairs[2];
+    int npairs = 0;
+    const cudaError_t e = resident_pairs[which].get(&npairs, [&](int &v) {
+      cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kPairSmemBytes));
+      if (r != cudaSuccess) return r;
       lc.gridDim = dim3(sms & ~1);
       int ncl = 0;
-      e = cudaOccupancyMaxActiveClusters(&ncl, kern, &lc);
-      if (e != cudaSuccess) return e;
+      r = cudaOccupancyMaxActiveClusters(&ncl, kern, &lc);
+      if (r != cudaSuccess) return r;
       if (ncl < 1) return cudaErrorInvalidConfiguration;
-      pairs[dev][which] = ncl < sms / 2 ? ncl : sms / 2;
-    }
-    lc.gridDim = dim3(2 * pairs[dev][which]);
+      v = ncl < sms / 2 ? ncl : sms / 2;
+      return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
+    lc.gridDim = dim3(2 * npairs);
     return cudaLaunchKernelEx(&lc, kern, tw, txp, g.offsets, g.rows_alloc, g.G, g.N, g.K,
                               static_cast<const __nv_bfloat16 *>(g.bias), g.act,
                               static_cast<__nv_bfloat16 *>(g.C),
                               static_cast<__nv_bfloat16 *>(g.pre),
                               static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
   }
-  static bool attr_set[2] = {false, false};
+  static PerDevice<int> smem_raised[2];
   const int which = g.b_kmajor ? 0 : 1;
   auto kern = g.b_kmajor ? tc_gemm_kernel<false> : tc_gemm_kernel<true>;
-  if (!attr_set[which]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set[which] = true;
-  }
+  int unused = 0;
+  if (const cudaError_t e = smem_raised[which].get(&unused, [&](int &) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kSmemBytes));
+      }); e != cudaSuccess)
+    return e;
   const int grid = sms;
   return launch_k(kern, grid, kThreads, kSmemBytes, st, tw, tx, g.offsets, g.rows_alloc, g.G,
                   g.N, g.K,

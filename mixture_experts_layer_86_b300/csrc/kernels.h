@@ -6,7 +6,44 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
+
+constexpr int kMaxDevices = 64;
+
+// Host state kept per CUDA device (a raised shared-memory limit, an
+// occupancy figure, a symbol address): one value per device, filled the
+// first time that device asks for it, under a lock, so host threads on the
+// same or on different devices never see a half-written entry.
+template <typename T>
+class PerDevice {
+ public:
+  // The value for the current device.  On first use `init(T &)` fills it;
+  // when init fails its error is returned and nothing is kept.
+  template <typename F>
+  cudaError_t get(T *out, F init) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!set_[dev]) {
+      T v{};
+      e = init(v);
+      if (e != cudaSuccess) return e;
+      val_[dev] = v;
+      set_[dev] = true;
+    }
+    *out = val_[dev];
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  bool set_[kMaxDevices] = {};
+  T val_[kMaxDevices] = {};
+};
 
 // Tokens per gate/routing CTA; the slot scan works on per-CTA histograms.
 constexpr int kRouteTokensPerCta = 128;

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 from _harness import DEV, GpuRun, WORKLOADS, assert_close, check_routing_equal, f64, oracle_cfg
+from mixture_experts_layer_86_b300 import _native as N
 from mixture_experts_layer_86_b300.inputs import make_inputs
 from oracle import moe_oracle as O
 
@@ -64,3 +65,26 @@ def test_backward_empty_expert_gets_zero_gradient():
         assert torch.all(run.grads[key][5] == 0), key
     ref, gref = _oracle_grads(run)
     _check_all(run, ref, gref)
+
+
+def test_training_step_every_element_full_size():
+    """The training configuration at its own size (S=8192, d=1024, E=32,
+    f=4096, ~512 rows per expert): the forward stages and all six gradients,
+    every element, against the oracle's forward and backward under the GPU's
+    routing.  At this size the weight-gradient GEMM runs 8 K blocks per tile
+    and the data-gradient GEMM two 256-token tiles per expert."""
+    wl = WORKLOADS["train_e32"]
+    run = GpuRun(wl, training=True)
+    run.backward()
+    assert N.moe_get_device_error() == 0
+    ref, gref = _oracle_grads(run)
+    check_routing_equal(run, ref)
+    R = run.num_rows
+    b = run.bufs
+    stats = {}
+    assert np.array_equal(f64(b["x_disp"][:R]), ref["x_disp"])
+    for key, name in (("h_pre", "h_pre"), ("h", "h"), ("out", "out_disp")):
+        stats[name] = assert_close(f64(b[name][:R]), ref[key], wl.dtype, name)
+    stats["y"] = assert_close(f64(run.y), ref["y"], wl.dtype, "y")
+    stats.update(_check_all(run, ref, gref))
+    print("train_e32 full size", {k: f"{v['rel_l2']:.2e}" for k, v in stats.items()})

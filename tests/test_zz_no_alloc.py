@@ -82,6 +82,28 @@ def test_static_gate_fp32_uses_builtin_logits_scratch():
         _same(ref, got, with_logits=False)
 
 
+def test_static_gate_allocates_no_device_memory():
+    """After the first call on the device (which looks up the scratch
+    array's address), further calls leave both torch's allocator and the
+    device's free memory exactly as they were."""
+    wl = Workload("gate_e64_mem", 4096, 2048, 64, 64, 2, 1.25, 4, True, "gelu_tanh", "bf16",
+                  seed=2)
+    cfg = N.config_from_workload(wl)
+    inp = make_inputs(wl).to(DEV)
+    got = _outputs(cfg, 0.0)
+    _call(N.moe_gate_topk_static, cfg, inp, got, True)
+    torch.cuda.synchronize()
+    allocated0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        _call(N.moe_gate_topk_static, cfg, inp, got, True)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == allocated0
+    assert free1 == free0, (free0, free1)
+    assert N.moe_get_device_error() == 0
+
+
 def test_static_gate_rejects_configs_beyond_its_scratch():
     cfg = N.make_config(1 << 20, 64, 64, 64, 2, 1.0, 4, True)   # S*E*4 = 256 MiB of logits
     fake = 1 << 44
