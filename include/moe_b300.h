@@ -115,7 +115,10 @@ typedef struct {
   int32_t *expert_offsets;/* [E+1] exclusive scan of kept_cnt               */
   int32_t *row_src;       /* [rows] s*k+j of the choice stored in each row  */
   float *l_aux;           /* [1] load-balancing loss                        */
-  void *x_disp;           /* [rows,d] T expert-major token copy             */
+  void *x_disp;           /* [rows,d] T expert-major token copy; NULL in a
+                             bf16 forward: the dispatch is then fused into
+                             the first expert GEMM (moe_expert_ffn_gather)
+                             and no copy is made.  moe_backward needs it. */
   void *h_pre;            /* [rows,f] T pre-activation (nullable forward)   */
   void *h;                /* [rows,f] T activation                          */
   void *out_disp;         /* [rows,d] T expert outputs                      */
@@ -224,6 +227,22 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_disp,
                           void *h_pre, void *h, void *out_disp,
                           moe_stream_t stream);
 
+/* Dispatch fused into the grouped expert FFN, for bf16 layers: the same
+ * h_pre, h and out_disp as moe_dispatch followed by moe_expert_ffn, bit for
+ * bit, without the expert-major copy x_disp.  The first GEMM reads row r of
+ * expert e's block straight from token row_src[r] / k of x into its operand
+ * ring (MoE explainer §3.1: dispatch, expert compute and combine fused, no
+ * flattened intermediate buffer; deepspeed.moe overview §3.4, fused
+ * kernels).  x: [S,d] T; row_src, expert_offsets: moe_gate_topk's outputs;
+ * the other arguments as moe_expert_ffn.  MOE_ERR_UNSUPPORTED for fp32
+ * layers and on a device with fewer than two SMs. */
+moe_status moe_expert_ffn_gather(const moe_config *cfg, const void *x,
+                                 const int32_t *row_src,
+                                 const int32_t *expert_offsets, const void *w1,
+                                 const void *b1, const void *w2, const void *b2,
+                                 void *h_pre, void *h, void *out_disp,
+                                 moe_stream_t stream);
+
 /* Combine (MoE explainer §3.1 Step 5 "gather weighted sum"; deepspeed.moe
  * overview §3.1 item 4): y[s] = sum over kept j of topk_w[s,j] *
  * out_disp[expert_offsets[e]+slot[s,j]], fp32 accumulation; a token with no
@@ -236,7 +255,9 @@ moe_status moe_combine(const moe_config *cfg, const void *out_disp,
 /* The whole forward pass (gate, dispatch, expert FFN, combine) on `stream`;
  * returns (y, l_aux, kept_cnt) like MoE.forward's (output, gate_loss,
  * expert_count), deepspeed.moe overview §2.1.  Every non-nullable field of
- * `buf` must be set (h_pre may be NULL when no backward follows).
+ * `buf` must be set (h_pre may be NULL when no backward follows; x_disp may
+ * be NULL for a bf16 layer, which fuses the dispatch into the first expert
+ * GEMM -- keep it set when moe_backward follows).
  * workspace: moe_workspace_size(cfg, 0) bytes. */
 moe_status moe_forward(const moe_config *cfg, const void *x,
                        const void *w_gate, const float *logit_bias,

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_gate_topk_static": (c_int, [POINTER(MoeConfig)] + [_P] * 13 + [_P]),
     "moe_dispatch": (c_int, [POINTER(MoeConfig)] + [_P] * 5 + [_P]),
     "moe_expert_ffn": (c_int, [POINTER(MoeConfig)] + [_P] * 9 + [_P]),
+    "moe_expert_ffn_gather": (c_int, [POINTER(MoeConfig)] + [_P] * 10 + [_P]),
     "moe_combine": (c_int, [POINTER(MoeConfig)] + [_P] * 6 + [_P]),
     "moe_forward": (c_int, [POINTER(MoeConfig)] + [_P] * 8 + [POINTER(MoeBuffers), _P,
                                                              c_size_t, _P]),
@@ -190,6 +191,15 @@ def moe_expert_ffn(cfg, x_disp, expert_offsets, w1, b1, w2, b2, h_pre, h, out_di
     _check("moe_expert_ffn", _lib.moe_expert_ffn(
         ctypes.byref(cfg), _ptr(x_disp), _ptr(expert_offsets), _ptr(w1), _ptr(b1), _ptr(w2),
         _ptr(b2), _ptr(h_pre), _ptr(h), _ptr(out_disp), _stream(stream)))
+
+
+def moe_expert_ffn_gather(cfg, x, row_src, expert_offsets, w1, b1, w2, b2, h_pre, h, out_disp,
+                          stream=None):
+    """The expert FFN with the dispatch fused into its first GEMM (token rows
+    read from x through row_src; no x_disp copy)."""
+    _check("moe_expert_ffn_gather", _lib.moe_expert_ffn_gather(
+        ctypes.byref(cfg), _ptr(x), _ptr(row_src), _ptr(expert_offsets), _ptr(w1), _ptr(b1),
+        _ptr(w2), _ptr(b2), _ptr(h_pre), _ptr(h), _ptr(out_disp), _stream(stream)))
 
 
 def moe_combine(cfg, out_disp, topk_idx, slot, expert_offsets, topk_w, y, stream=None):

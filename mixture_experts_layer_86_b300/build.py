@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_b300.so")
 
 SOURCES = ["api.cu", "route.cu", "dispatch.cu", "gemm_simt.cu", "gemm_tc.cu", "gate_tc.cu",
-           "gate_static.cu", "backward.cu"]
+           "gate_route.cu", "gate_static.cu", "backward.cu"]
 HEADERS = ["common.cuh", "kernels.h", "tc_ptx.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -184,6 +184,45 @@ moe_status expert_ffn(const moe_config *c, const void *x_disp, const int32_t *of
   return cuda_status(launch_simt_gemm(g2, st));
 }
 
+// The expert FFN with the dispatch fused into its first GEMM: row r of the
+// grouped operand is token row_src[r] / k of x (bf16 layers only).
+moe_status expert_ffn_gather(const moe_config *c, const void *x, const int32_t *row_src,
+                             const int32_t *offsets, const void *w1, const void *b1,
+                             const void *w2, const void *b2, void *h_pre, void *h, void *out,
+                             cudaStream_t st) {
+  if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const int64_t R = max_rows_of(c);
+  const int d = c->hidden_size, f = c->ffn_size, E = c->num_experts;
+  if (R == 0) return MOE_OK;
+  TcGemm g1{};
+  g1.A = x; g1.rows_alloc = c->num_tokens; g1.B = w1; g1.b_kmajor = true; g1.C = h;
+  g1.N = f; g1.K = d; g1.G = E; g1.offsets = offsets; g1.bias = b1; g1.act = c->act;
+  g1.pre = h_pre; g1.grad_src = nullptr; g1.dact = 0; g1.err = device_error_ptr();
+  g1.row_src = row_src; g1.k_choices = c->k;
+  const cudaError_t e = launch_tc_gemm(g1, st);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  MOE_CUDA(e);
+  TcGemm g2{};
+  g2.A = h; g2.rows_alloc = R; g2.B = w2; g2.b_kmajor = true; g2.C = out;
+  g2.N = d; g2.K = f; g2.G = E; g2.offsets = offsets; g2.bias = b2; g2.act = -1;
+  g2.err = device_error_ptr();
+  return cuda_status(launch_tc_gemm(g2, st));
+}
+
+// Dispatch then the expert FFN, or -- when the caller passes no x_disp --
+// the FFN with the dispatch fused into its first GEMM.
+moe_status dispatch_and_ffn(const moe_config *c, const void *x, const moe_buffers *buf,
+                            const void *w1, const void *b1, const void *w2, const void *b2,
+                            cudaStream_t st) {
+  if (!buf->x_disp)
+    return expert_ffn_gather(c, x, buf->row_src, buf->expert_offsets, w1, b1, w2, b2, buf->h_pre,
+                             buf->h, buf->out_disp, st);
+  MOE_CUDA(launch_dispatch(x, c->dtype, c->num_tokens, c->hidden_size, c->k, buf->topk_idx,
+                           buf->slot, buf->expert_offsets, buf->x_disp, st));
+  return expert_ffn(c, buf->x_disp, buf->expert_offsets, w1, b1, w2, b2, buf->h_pre, buf->h,
+                    buf->out_disp, st);
+}
+
 // The residual expert of PR-MoE on every token: h = act(x rw1^T + rb1),
 // out = h rw2^T + rb2 -- the grouped GEMM with one group of all S rows.
 moe_status dense_mlp(const moe_config *c, const void *x, const void *rw1, const void *rb1,
@@ -299,7 +338,19 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x, const void *w_gat
     return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < fwd_ws_bytes(cfg)) return MOE_ERR_WORKSPACE;
   if (cfg->dtype == MOE_BF16) {
-    // fused tensor-core gate, then the shared scan / assignment
+    // one launch: tensor-core gate, routing and slot assignment
+    GateRouteArgs ga{};
+    ga.x = x; ga.w_gate = w_gate; ga.S = cfg->num_tokens; ga.d = cfg->hidden_size;
+    ga.E = cfg->num_experts; ga.k = cfg->k; ga.cap = capacity_of(cfg);
+    ga.rows_alloc = max_rows_of(cfg);
+    ga.logit_bias = logit_bias; ga.bias_ld = cfg->logit_bias_per_token ? cfg->num_experts : 0;
+    ga.inv_temp = inv_temperature(cfg); ga.aux_type = cfg->aux_loss_type;
+    ga.logits = logits; ga.probs = probs; ga.idx = topk_idx; ga.w = topk_w; ga.slot = slot;
+    ga.routed = routed_cnt; ga.kept = kept_cnt; ga.offsets = expert_offsets; ga.row_src = row_src;
+    ga.l_aux = l_aux; ga.ws = workspace; ga.ws_bytes = workspace_bytes; ga.err = device_error_ptr();
+    const cudaError_t ge = launch_gate_route(ga, stream);
+    if (ge != cudaErrorNotSupported) return cuda_status(ge);
+    // larger batches: fused tensor-core gate, then the shared scan / assignment
     RouteArgs a{};
     a.S = cfg->num_tokens; a.E = cfg->num_experts; a.k = cfg->k; a.cap = capacity_of(cfg);
     a.inv_temp = inv_temperature(cfg);
@@ -348,6 +399,18 @@ moe_status moe_expert_ffn(const moe_config *cfg, const void *x_disp,
   return expert_ffn(cfg, x_disp, expert_offsets, w1, b1, w2, b2, h_pre, h, out_disp, stream);
 }
 
+moe_status moe_expert_ffn_gather(const moe_config *cfg, const void *x, const int32_t *row_src,
+                                 const int32_t *expert_offsets, const void *w1, const void *b1,
+                                 const void *w2, const void *b2, void *h_pre, void *h,
+                                 void *out_disp, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (!ok_ptr(x) || !ok_ptr(row_src) || !ok_ptr(expert_offsets) || !ok_ptr(w1) || !ok_ptr(b1) ||
+      !ok_ptr(w2) || !ok_ptr(b2) || !ok_opt(h_pre) || !ok_ptr(h) || !ok_ptr(out_disp))
+    return MOE_ERR_INVALID_ARG;
+  return expert_ffn_gather(cfg, x, row_src, expert_offsets, w1, b1, w2, b2, h_pre, h, out_disp,
+                           stream);
+}
+
 moe_status moe_combine(const moe_config *cfg, const void *out_disp, const int32_t *topk_idx,
                        const int32_t *slot, const int32_t *expert_offsets, const float *topk_w,
                        void *y, moe_stream_t stream) {
@@ -364,17 +427,15 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *w_gate,
                        const void *b2, void *y, const moe_buffers *buf, void *workspace,
                        size_t workspace_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
-  if (!buf || !ok_ptr(y) || !ok_ptr(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
+  if (!buf || !ok_ptr(y) || !ok_opt(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
       !ok_opt(buf->h_pre) || !ok_ptr(w1) || !ok_ptr(b1) || !ok_ptr(w2) || !ok_ptr(b2))
     return MOE_ERR_INVALID_ARG;
+  if (!buf->x_disp && cfg->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   MOE_TRY(moe_gate_topk(cfg, x, w_gate, logit_bias, buf->logits, buf->probs, buf->topk_idx,
                         buf->topk_w, buf->slot, buf->routed_cnt, buf->kept_cnt,
                         buf->expert_offsets, buf->row_src, buf->l_aux, workspace, workspace_bytes,
                         stream));
-  MOE_CUDA(launch_dispatch(x, cfg->dtype, cfg->num_tokens, cfg->hidden_size, cfg->k,
-                           buf->topk_idx, buf->slot, buf->expert_offsets, buf->x_disp, stream));
-  MOE_TRY(expert_ffn(cfg, buf->x_disp, buf->expert_offsets, w1, b1, w2, b2, buf->h_pre, buf->h,
-                     buf->out_disp, stream));
+  MOE_TRY(dispatch_and_ffn(cfg, x, buf, w1, b1, w2, b2, stream));
   return cuda_status(launch_combine(buf->out_disp, cfg->dtype, cfg->num_tokens, cfg->hidden_size,
                                     cfg->k, buf->topk_idx, buf->slot, buf->expert_offsets,
                                     buf->topk_w, y, stream));
@@ -388,11 +449,12 @@ moe_status moe_forward_residual(const moe_config *cfg, const void *x, const void
                                 void *res_h, void *res_out, void *workspace,
                                 size_t workspace_bytes, moe_stream_t stream) {
   MOE_TRY(check_config(cfg));
-  if (!buf || !ok_ptr(y) || !ok_ptr(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
+  if (!buf || !ok_ptr(y) || !ok_opt(buf->x_disp) || !ok_ptr(buf->h) || !ok_ptr(buf->out_disp) ||
       !ok_opt(buf->h_pre) || !ok_ptr(w1) || !ok_ptr(b1) || !ok_ptr(w2) || !ok_ptr(b2) ||
       !ok_ptr(rw1) || !ok_ptr(rb1) || !ok_ptr(rw2) || !ok_ptr(rb2) || !ok_ptr(res_h) ||
       !ok_ptr(res_out) || !ok_opt(mix_w))
     return MOE_ERR_INVALID_ARG;
+  if (!buf->x_disp && cfg->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   // the learned mix takes all three of its arguments, the sum none of them
   if (mix_w ? (!ok_ptr(mix_b) || !ok_ptr(mix)) : (mix_b != nullptr || mix != nullptr))
     return MOE_ERR_INVALID_ARG;
@@ -403,10 +465,7 @@ moe_status moe_forward_residual(const moe_config *cfg, const void *x, const void
                         buf->topk_w, buf->slot, buf->routed_cnt, buf->kept_cnt,
                         buf->expert_offsets, buf->row_src, buf->l_aux, workspace, workspace_bytes,
                         stream));
-  MOE_CUDA(launch_dispatch(x, cfg->dtype, cfg->num_tokens, cfg->hidden_size, cfg->k,
-                           buf->topk_idx, buf->slot, buf->expert_offsets, buf->x_disp, stream));
-  MOE_TRY(expert_ffn(cfg, buf->x_disp, buf->expert_offsets, w1, b1, w2, b2, buf->h_pre, buf->h,
-                     buf->out_disp, stream));
+  MOE_TRY(dispatch_and_ffn(cfg, x, buf, w1, b1, w2, b2, stream));
   MOE_TRY(dense_mlp(cfg, x, rw1, rb1, rw2, rb2, res_h, res_out, stream));
   return cuda_status(launch_combine(buf->out_disp, cfg->dtype, cfg->num_tokens, cfg->hidden_size,
                                     cfg->k, buf->topk_idx, buf->slot, buf->expert_offsets,
@@ -434,12 +493,21 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
   // 1. dO = w * dY per kept row; dw = <dY, out>
   MOE_CUDA(launch_combine_bwd(dy, sv->out_disp, dt, S, d, k, sv->topk_idx, sv->slot,
                               sv->expert_offsets, sv->topk_w, w.d_out, w.dw, st));
-  // 2. dW2_e = dO_e^T h_e ; db2 = column sums of dO
+  // 2. dW2_e = dO_e^T h_e ; db2 = column sums of dO (in the same kernel
+  //    when the CTA-pair weight-gradient GEMM runs)
+  bool db2_done = false;
   if (dt == MOE_BF16) {
     TcWgrad g{};
     g.A = w.d_out; g.B = sv->h; g.rows_alloc = R > 0 ? R : 1; g.C = dw2;
     g.M = d; g.N = f; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
-    MOE_CUDA(launch_tc_wgrad(g, st));
+    g.colsum = db2;
+    cudaError_t e = launch_tc_wgrad(g, st);
+    db2_done = e == cudaSuccess;
+    if (e == cudaErrorNotSupported) {
+      g.colsum = nullptr;
+      e = launch_tc_wgrad(g, st);
+    }
+    MOE_CUDA(e);
   } else {
     SimtGemm g{};
     g.a_dtype = g.b_dtype = g.c_dtype = dt;
@@ -450,7 +518,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     g.act = -1;
     MOE_CUDA(launch_simt_gemm(g, st));
   }
-  MOE_CUDA(launch_group_colsum(w.d_out, dt, d, E, sv->expert_offsets, db2, st));
+  if (!db2_done) MOE_CUDA(launch_group_colsum(w.d_out, dt, d, E, sv->expert_offsets, db2, st));
   // 3. dh_pre = (dO W2_e) * act'(h_pre)
   if (R > 0) {
     if (dt == MOE_BF16) {
@@ -471,11 +539,19 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     }
   }
   // 4. dW1_e = dh_pre_e^T x_disp_e ; db1 = column sums of dh_pre
+  bool db1_done = false;
   if (dt == MOE_BF16) {
     TcWgrad g{};
     g.A = w.dh_pre; g.B = sv->x_disp; g.rows_alloc = R > 0 ? R : 1; g.C = dw1;
     g.M = f; g.N = d; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
-    MOE_CUDA(launch_tc_wgrad(g, st));
+    g.colsum = db1;
+    cudaError_t e = launch_tc_wgrad(g, st);
+    db1_done = e == cudaSuccess;
+    if (e == cudaErrorNotSupported) {
+      g.colsum = nullptr;
+      e = launch_tc_wgrad(g, st);
+    }
+    MOE_CUDA(e);
   } else {
     SimtGemm g{};
     g.a_dtype = g.b_dtype = g.c_dtype = dt;
@@ -486,7 +562,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     g.act = -1;
     MOE_CUDA(launch_simt_gemm(g, st));
   }
-  MOE_CUDA(launch_group_colsum(w.dh_pre, dt, f, E, sv->expert_offsets, db1, st));
+  if (!db1_done) MOE_CUDA(launch_group_colsum(w.dh_pre, dt, f, E, sv->expert_offsets, db1, st));
   // 5. dx_disp = dh_pre W1_e
   if (R > 0) {
     if (dt == MOE_BF16) {

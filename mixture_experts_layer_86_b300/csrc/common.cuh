@@ -202,6 +202,8 @@ enum : uint32_t {
   kErrWgradMma = 0x09000000u,
   kErrWgradEpilogue = 0x0a000000u,
   kErrWgradFixup = 0x0b000000u,
+  kErrGateBarrier = 0x0c000000u,
+  kErrGemmGather = 0x0d000000u,
 };
 
 __device__ __forceinline__ void record_error(unsigned int *err, uint32_t code) {

@@ -1,0 +1,682 @@
+// Single-launch gate for bf16 layers: router GEMM on the tensor cores,
+// softmax, top-k, combine weights AND the capacity-limited slot assignment,
+// counts, offsets and l_aux, in one kernel.
+//
+// MoE explainer (lpnh.cn/news/725941) §3.1 Steps 1-2 (router linear layer,
+// top-k, softmax over the selected logits); DeepSeek-MoE page
+// (lnwmold.com/news/1162317) ch.1 (softmax -> top-2, capacity =
+// ceil(S*2/E*cf)); deepspeed.moe overview (adg.csdn.net/694deb285b9f5f31781ae763)
+// §2.1 (min_capacity, drop_tokens, gate_loss, expert_count).
+//
+// The stage is bound by reading x once from HBM.  Every CTA takes one tile
+// of TM tokens, TM = ceil(S / #SMs) rounded up to 8 rows (at most 128), so
+// every SM streams its share of x at the same time; the kernel is launched
+// cooperatively (all CTAs resident), one CTA per SM.
+//
+// Phase A, per tile:
+//   warp 0     TMA producer: x tile (TM x 64 per box) and W_g tile
+//              (E x 64 per box) K-slices into a shared-memory ring
+//   warp 1     TMEM allocator + MMA issuer: tcgen05.mma M = 128 (rows
+//              past TM are zero), N = E rounded up to 16, fp32 in TMEM
+//   warps 4-7  one token per thread, its logits read straight from TMEM
+//              (lane = token): top-2 with ties to the lower expert index,
+//              softmax of logits / T, combine weights; the tile's
+//              per-expert probability sums (column sums through a
+//              shared-memory transpose, fixed order); per (choice j,
+//              expert e) the tile's count and each token's rank among the
+//              tile's tokens with the same (j, e), in token order
+//              (__match_any_sync within a warp, warp prefixes across).
+//   The tile's counts and probability sums go to the workspace.
+// Grid barrier (bounded wait).
+// Phase B, every CTA for its own tile, in parallel: the counts of all
+//   tiles give this tile's prefix (the tiles before it) and the totals;
+//   slot = prefix[j][e] + (j == 1 ? first-choice total of e : 0) + rank,
+//   dropped at >= capacity.  Every first choice therefore precedes every
+//   second choice, each in token order (the GShard priority order of the
+//   layer's specification).  Tile 0 writes the routed / kept counts, the
+//   expert offsets (exclusive scan of kept) and l_aux.
+// Everything is deterministic: integer counts, probability sums added in
+// a fixed order and then as exact 2^-30 fixed-point integers.
+#include <cuda.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+// Barrier words of the gate's grid-wide barrier: the number of CTAs that
+// have arrived and a generation.  Zero when the module loads; the last CTA
+// to arrive resets the count before it bumps the generation, so the words
+// are (0, g+1) after every launch.  Launches take the slots in turn, so
+// gate launches that overlap on the GPU (different streams) use different
+// words as long as fewer than kGateBarrierSlots of them overlap.
+struct GridBarrierWords {
+  unsigned int count;
+  unsigned int gen;
+};
+constexpr int kGateBarrierSlots = 64;
+__device__ GridBarrierWords g_gate_barrier[kGateBarrierSlots];
+
+namespace {
+
+constexpr int kGrThreads = 256;                 // 8 warps
+constexpr int kGrMaxStages = 8;
+constexpr int kGrMaxTile = 128;
+constexpr uint32_t kXBoxBytes = 128 * 128;      // 128 token rows x 64 bf16; TM rows loaded
+constexpr uint32_t kStgFloats = 32 * 33;        // one epilogue warp's transpose tile
+constexpr uint64_t kGrWaitNs = 2000000000ull;   // 2 s
+#ifndef MOE_GATE_BOXES
+#define MOE_GATE_BOXES 1                        // 64-wide K boxes per ring stage
+#endif
+
+struct __align__(16) GrCtl {
+  uint64_t full[kGrMaxStages];
+  uint64_t empty[kGrMaxStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+  int barrier_ok;
+  float bias[kMaxExperts];          // the [E] logit bias (zero without one)
+  float psum_w[4][kMaxExperts];     // per-warp probability sums of the tile
+  int32_t wcnt[4][kMaxExperts];     // per-warp counts, then warp prefixes
+  int32_t cnt[2][kMaxExperts];      // this tile's count per (j, e)
+  int32_t pre[2][kMaxExperts];      // counts of the tiles before this one
+  int32_t tot[2][kMaxExperts];      // counts of all tiles
+  int32_t offs[kMaxExperts + 1];    // expert offsets
+  int32_t choice[2][kGrMaxTile];    // chosen expert per (j, token), -1 none
+  int32_t rank[2][kGrMaxTile];      // rank among the tile's (j, e) tokens
+  long long aux[kMaxExperts];       // sum over tokens of p[., e], 2^-30 units
+};
+
+struct GrParams {
+  int64_t S;
+  int d, E, E_pad, k, TM, ntiles, nbox, nstages, nk, nk64;
+  uint32_t idesc, tmem_cols, stage_bytes;
+  int64_t cap;          // -1: no capacity
+  int64_t rows_alloc;   // rows of the expert-major buffers
+  const float *logit_bias;
+  int bias_ld;          // 0: [E] bias; E: [S,E] bias
+  float inv_temp;
+  int aux_type;
+  float *logits, *probs;
+  int32_t *idx;
+  float *w;
+  int32_t *slot;
+  int32_t *routed, *kept, *offsets, *row_src;
+  float *l_aux;
+  int32_t *hist;        // [ntiles][hist_pitch] counts per (j, e)
+  float *psum;          // [ntiles][psum_pitch] probability sums per e
+  int hist_pitch, psum_pitch;
+  unsigned int *err;
+  unsigned int barrier_slot;
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier; thread 0 of every CTA calls it once, after a block
+// barrier.  Returns false when it waited longer than limit_ns (the CTA has
+// still arrived, so the words stay consistent for the next launch).
+__device__ bool grid_barrier(GridBarrierWords *b, unsigned int nblocks, uint64_t limit_ns) {
+  __threadfence();  // this CTA's global writes are visible before it arrives
+  const unsigned int gen0 = ld_acquire_gpu(&b->gen);
+  const unsigned int t = atomicAdd(&b->count, 1u);
+  if (t == nblocks - 1) {
+    atomicExch(&b->count, 0u);
+    __threadfence();
+    atomicAdd(&b->gen, 1u);
+    return true;
+  }
+  const uint64_t t0 = ptx::globaltimer();
+  while (ld_acquire_gpu(&b->gen) == gen0) {
+    __nanosleep(64);
+    if (ptx::globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ int4 add4(int4 a, int4 b) {
+  return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ int comp4(const int4 &v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(kGrThreads, 1)
+gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  const __grid_constant__ GrParams p) {
+  griddep_begin();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  GrCtl &ctl = *reinterpret_cast<GrCtl *>(ring + size_t(p.nstages) * p.stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x;
+  const int64_t tok0 = int64_t(tile) * p.TM;
+  const int E = p.E, k = p.k;
+  const uint32_t wbox_bytes = uint32_t(p.E_pad) * 128;
+
+  // ---------------------------------------------------------------- setup
+  if (tid == 0) {
+    for (int s = 0; s < p.nstages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.done), 1);
+    ctl.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmX);
+    ptx::tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), p.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  // the [E] bias, and zeros in the x-box rows past TM that the M = 128 MMA
+  // reads (written once; the TMA copies never touch them)
+  for (int e = tid; e < kMaxExperts; e += kGrThreads)
+    ctl.bias[e] = (p.logit_bias != nullptr && p.bias_ld == 0 && e < E) ? p.logit_bias[e] : 0.0f;
+  if (p.TM < kGrMaxTile) {
+    const uint32_t pad = (kGrMaxTile - p.TM) * 128;  // bytes past the TM rows of one box
+    const uint32_t per_box = pad / 16;
+    const uint32_t n = uint32_t(p.nstages * p.nbox) * per_box;
+    for (uint32_t i = tid; i < n; i += kGrThreads) {
+      const uint32_t box = i / per_box, off = (i - box * per_box) * 16;
+      const uint32_t st = box / p.nbox, b = box - st * p.nbox;
+      *reinterpret_cast<uint4 *>(ring + st * p.stage_bytes + b * kXBoxBytes + p.TM * 128 + off) =
+          make_uint4(0, 0, 0, 0);
+    }
+    ptx::fence_proxy_async_smem();  // visible to the tensor cores' reads
+  }
+  ptx::tc_fence_before();
+  block_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int *abort = &ctl.abort;
+
+  // ------------------------------------------------------------ phase A
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < p.nk; ++kb) {
+        const int stage = kb % p.nstages;
+        const uint32_t phase = (kb / p.nstages) & 1;
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kGrWaitNs)) {
+          record_error(p.err, kErrGateProducer | uint32_t(tile & 0xffffff));
+          *abort = 1;
+          ok = false;
+          break;
+        }
+        const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
+        const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
+        uint8_t *st = ring + stage * p.stage_bytes;
+        ptx::mbar_arrive_expect_tx(fb, uint32_t(nb) * (uint32_t(p.TM) * 128 + wbox_bytes));
+        for (int b = 0; b < nb; ++b) {
+          const int k0 = (kb * p.nbox + b) * 64;
+          ptx::tma_load_2d(ptx::smem_addr(st + b * kXBoxBytes), &tmX, fb, k0, int32_t(tok0));
+          ptx::tma_load_2d(ptx::smem_addr(st + p.nbox * kXBoxBytes + b * wbox_bytes), &tmW, fb,
+                           k0, 0);
+        }
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+      }
+      if (!ok)  // copies already issued land before the ring is reused
+        for (int s = 0; s < p.nstages; ++s)
+          if (armed & (1u << s))
+            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+                           kGrWaitNs / 4);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t desc0 = ptx::sdesc_sw128(ptx::smem_addr(ring), 16, 1024);
+      bool ok = true;
+      for (int kb = 0; kb < p.nk; ++kb) {
+        const int stage = kb % p.nstages;
+        const uint32_t phase = (kb / p.nstages) & 1;
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kGrWaitNs)) {
+          record_error(p.err, kErrGateMma | uint32_t(tile & 0xffffff));
+          *abort = 1;
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
+        const uint64_t sdesc = ptx::sdesc_add(desc0, stage * p.stage_bytes);
+        for (int b = 0; b < nb; ++b) {
+          const uint64_t ad = ptx::sdesc_add(sdesc, b * kXBoxBytes);
+          const uint64_t bd = ptx::sdesc_add(sdesc, p.nbox * kXBoxBytes + b * wbox_bytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16(tmem, ptx::sdesc_add(ad, kk * 32), ptx::sdesc_add(bd, kk * 32), p.idesc,
+                          (kb | b | kk) != 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
+      }
+      ptx::mma_commit(ptx::smem_addr(&ctl.done));
+      // after a give-up, the MMAs already issued finish before TMEM is freed
+      if (!ok) ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, nullptr, kGrWaitNs / 4);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------- epilogue: lane = token
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int r = q * 32 + lane;
+    const int64_t s = tok0 + r;
+    const bool valid = r < p.TM && s < p.S;
+    if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, kGrWaitNs)) {
+      record_error(p.err, kErrGateEpilogue | uint32_t(tile & 0xffffff));
+      *abort = 1;
+    }
+    ptx::tc_fence_after();
+    // the ring is idle once every MMA is done: each warp's transpose tile
+    float *stg = reinterpret_cast<float *>(ring) + q * kStgFloats;
+    const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+    const float *brow = (p.logit_bias != nullptr && p.bias_ld != 0 && valid)
+                            ? p.logit_bias + s * p.bias_ld
+                            : nullptr;
+    const int nchunk = (E + 31) >> 5;
+    const int64_t wrow0 = tok0 + q * 32;  // first token of this warp's rows
+    // valid rows of this warp (<= 0 when the warp's lanes are all past the tile)
+    int64_t wr = p.S - wrow0;
+    if (wr > p.TM - q * 32) wr = p.TM - q * 32;
+    const int wrows = wr > 32 ? 32 : int(wr);
+
+    // pass 1: top-2 (ties to the lower index) and the optional logits rows
+    float b1 = -INFINITY, b2 = -INFINITY;
+    int i1 = -1, i2 = -1;
+    for (int c = 0; c < nchunk; ++c) {
+      uint32_t raw[32];
+      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int e = c * 32 + t;
+        if (e < E) {
+          const float v = __uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]);
+          if (i1 < 0 || v > b1) {
+            b2 = b1;
+            i2 = i1;
+            b1 = v;
+            i1 = e;
+          } else if (i2 < 0 || v > b2) {
+            b2 = v;
+            i2 = e;
+          }
+          if (p.logits) stg[lane * 33 + t] = v;
+        }
+      }
+      if (p.logits) {
+        __syncwarp();
+        const int e = c * 32 + lane;
+        for (int rr = 0; rr < wrows; ++rr)
+          if (e < E) p.logits[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
+        __syncwarp();
+      }
+    }
+    // pass 2: the softmax normaliser (the top-1 logit is the shift)
+    const float m = b1;
+    float z = 0.0f;
+    for (int c = 0; c < nchunk; ++c) {
+      uint32_t raw[32];
+      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int e = c * 32 + t;
+        if (e < E)
+          z += expf((__uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]) - m) * p.inv_temp);
+      }
+    }
+    const float inv_z = 1.0f / z;
+    // pass 3: probabilities (0 for rows past the batch), the tile's column
+    // sums and the optional probability rows
+    for (int c = 0; c < nchunk; ++c) {
+      uint32_t raw[32];
+      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int e = c * 32 + t;
+        float pv = 0.0f;
+        if (e < E && valid)
+          pv = expf((__uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]) - m) * p.inv_temp) *
+               inv_z;
+        stg[lane * 33 + t] = pv;
+      }
+      __syncwarp();
+      const int e = c * 32 + lane;
+      float cs = 0.0f;
+      for (int rr = 0; rr < 32; ++rr) cs += stg[rr * 33 + lane];
+      if (e < E) ctl.psum_w[q][e] = cs;
+      if (p.probs)
+        for (int rr = 0; rr < wrows; ++rr)
+          if (e < E) p.probs[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
+      __syncwarp();
+    }
+    ptx::tc_fence_before();
+    if (valid) {
+      p.idx[s * k] = i1;
+      if (k == 1) {
+        p.w[s] = inv_z;  // exp(l1 - max) = 1
+      } else {
+        const float x2 = expf((b2 - m) * p.inv_temp);
+        const float den = 1.0f + x2;
+        p.w[s * 2] = 1.0f / den;
+        p.w[s * 2 + 1] = x2 / den;
+        p.idx[s * 2 + 1] = i2;
+      }
+    }
+    ctl.choice[0][r] = valid ? i1 : -1;
+    ctl.choice[1][r] = (valid && k == 2) ? i2 : -1;
+
+    // the tile's count and each token's rank per (j, e), in token order
+    const int et = tid - 128;  // 0..127 over warps 4..7
+    for (int j = 0; j < k; ++j) {
+      for (int i = et; i < 4 * kMaxExperts; i += 128) (&ctl.wcnt[0][0])[i] = 0;
+      epi_sync();
+      const int e = ctl.choice[j][r];
+      const unsigned peers = __match_any_sync(kFullMask, e);
+      const int rk = __popc(peers & lanemask_lt());
+      if (e >= 0 && rk == 0) ctl.wcnt[q][e] = __popc(peers);
+      epi_sync();
+      for (int ee = et; ee < E; ee += 128) {
+        int run = 0;
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int cnum = ctl.wcnt[w4][ee];
+          ctl.wcnt[w4][ee] = run;
+          run += cnum;
+        }
+        ctl.cnt[j][ee] = run;
+      }
+      epi_sync();
+      ctl.rank[j][r] = e >= 0 ? ctl.wcnt[q][e] + rk : 0;
+      epi_sync();
+    }
+    // publish the tile's counts and probability sums (padding entries 0)
+    for (int i = et; i < p.hist_pitch; i += 128)
+      p.hist[int64_t(tile) * p.hist_pitch + i] = i < k * E ? ctl.cnt[i / E][i % E] : 0;
+    for (int e = et; e < p.psum_pitch; e += 128)
+      p.psum[int64_t(tile) * p.psum_pitch + e] =
+          e < E ? ((ctl.psum_w[0][e] + ctl.psum_w[1][e]) + ctl.psum_w[2][e]) + ctl.psum_w[3][e]
+                : 0.0f;
+  }
+
+  ptx::tc_fence_before();
+  block_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, p.tmem_cols);
+  }
+
+  // ------------------------------------------------------- grid barrier
+  if (tid == 0) {
+    const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles), kGrWaitNs);
+    if (!ok) record_error(p.err, kErrGateBarrier | uint32_t(tile & 0xffffff));
+    ctl.barrier_ok = ok ? 1 : 0;
+  }
+  block_sync();
+  // Without the barrier some tiles' counts may be missing: every choice of
+  // this tile is then dropped and tile 0 reports empty experts.
+  const bool okb = ctl.barrier_ok != 0;
+
+  // ------------------------------------------------------------ phase B
+  // prefix and totals of the per-tile counts, 4 columns per load
+  {
+    const int nv = p.hist_pitch >> 2;
+    const int RG = max(1, kGrThreads / nv);
+    const int v = tid % nv, g = tid / nv;
+    int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+    const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
+    if (g < RG && okb) {
+      int t = g;
+      for (; t + 3 * RG < p.ntiles; t += 4 * RG) {
+        const int4 a0 = __ldcg(h4 + int64_t(t) * nv + v);
+        const int4 a1 = __ldcg(h4 + int64_t(t + RG) * nv + v);
+        const int4 a2 = __ldcg(h4 + int64_t(t + 2 * RG) * nv + v);
+        const int4 a3 = __ldcg(h4 + int64_t(t + 3 * RG) * nv + v);
+        tot = add4(add4(tot, a0), add4(a1, add4(a2, a3)));
+        if (t < tile) pre = add4(pre, a0);
+        if (t + RG < tile) pre = add4(pre, a1);
+        if (t + 2 * RG < tile) pre = add4(pre, a2);
+        if (t + 3 * RG < tile) pre = add4(pre, a3);
+      }
+      for (; t < p.ntiles; t += RG) {
+        const int4 a0 = __ldcg(h4 + int64_t(t) * nv + v);
+        tot = add4(tot, a0);
+        if (t < tile) pre = add4(pre, a0);
+      }
+    }
+    int4 *red = reinterpret_cast<int4 *>(ring);  // [2][RG][nv]
+    if (g < RG) {
+      red[g * nv + v] = pre;
+      red[RG * nv + g * nv + v] = tot;
+    }
+    block_sync();
+    for (int i = tid; i < k * E; i += kGrThreads) {
+      const int vi = i >> 2, c = i & 3;
+      int P = 0, T = 0;
+      for (int gg = 0; gg < RG; ++gg) {
+        P += comp4(red[gg * nv + vi], c);
+        T += comp4(red[RG * nv + gg * nv + vi], c);
+      }
+      ctl.pre[i / E][i % E] = P;
+      ctl.tot[i / E][i % E] = T;
+    }
+    block_sync();
+  }
+  // routed / kept counts and the expert offsets (warp 0; lane l owns a
+  // contiguous range of experts)
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
+      local += (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
+      const int kp = (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
+      // offsets never pass the rows the buffers hold (true by construction
+      // when every tile's counts arrived)
+      ctl.offs[e] = run < p.rows_alloc ? run : int(p.rows_alloc);
+      if (tile == 0) {
+        p.routed[e] = rt;
+        p.kept[e] = kp;
+        p.offsets[e] = ctl.offs[e];
+      }
+      run += kp;
+    }
+    if (lane == 31) {
+      ctl.offs[E] = incl < p.rows_alloc ? incl : int(p.rows_alloc);
+      if (tile == 0) p.offsets[E] = ctl.offs[E];
+    }
+  }
+  block_sync();
+  // final slots and the row map of this tile's choices
+  for (int i = tid; i < p.TM * k; i += kGrThreads) {
+    const int r = i / k, j = i - r * k;
+    const int64_t s = tok0 + r;
+    if (s >= p.S) continue;
+    const int e = ctl.choice[j][r];
+    int pos = -1;
+    if (okb && e >= 0) {
+      pos = ctl.pre[j][e] + (j == 1 ? ctl.tot[0][e] : 0) + ctl.rank[j][r];
+      if (pos >= ctl.offs[e + 1] - ctl.offs[e]) pos = -1;  // beyond the capacity
+    }
+    p.slot[s * k + j] = pos;
+    if (pos >= 0) p.row_src[ctl.offs[e] + pos] = int32_t(s * k + j);
+  }
+  // l_aux (tile 0): probability sums over all tiles, as exact fixed-point
+  if (tile == 0) {
+    const int nv = p.psum_pitch >> 2;
+    const int RG = max(1, kGrThreads / nv);
+    const int v = tid % nv, g = tid / nv;
+    long long a[4] = {0, 0, 0, 0};
+    const float4 *p4 = reinterpret_cast<const float4 *>(p.psum);
+    if (g < RG && okb)
+      for (int t = g; t < p.ntiles; t += RG) {
+        const float4 f = __ldcg(p4 + int64_t(t) * nv + v);
+        a[0] += __float2ll_rn(f.x * 1073741824.0f);
+        a[1] += __float2ll_rn(f.y * 1073741824.0f);
+        a[2] += __float2ll_rn(f.z * 1073741824.0f);
+        a[3] += __float2ll_rn(f.w * 1073741824.0f);
+      }
+    // the count reduction above is done with the ring: reuse it
+    long long *red = reinterpret_cast<long long *>(ring);  // [RG][psum_pitch]
+    if (g < RG)
+      for (int c = 0; c < 4; ++c) red[g * p.psum_pitch + v * 4 + c] = a[c];
+    block_sync();
+    for (int e = tid; e < E; e += kGrThreads) {
+      long long t = 0;
+      for (int gg = 0; gg < RG; ++gg) t += red[gg * p.psum_pitch + e];
+      ctl.aux[e] = t;
+    }
+    block_sync();
+    if (warp == 0) {
+      const int per = (E + 31) / 32;
+      const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+      const double S = double(p.S);
+      double aux = 0.0;
+      for (int e = e0; e < e1; ++e)
+        aux += double(ctl.aux[e]) * (1.0 / 1073741824.0) * double(ctl.tot[0][e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
+      if (p.aux_type == MOE_AUX_STD) {
+        // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
+        double su = 0.0, sq = 0.0;
+        for (int e = e0; e < e1; ++e) su += double(ctl.aux[e]) * (1.0 / 1073741824.0) / S;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(kFullMask, su, o);
+        const double mean = su / double(E);
+        for (int e = e0; e < e1; ++e) {
+          const double dv = double(ctl.aux[e]) * (1.0 / 1073741824.0) / S - mean;
+          sq += dv * dv;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
+        if (lane == 0) *p.l_aux = okb ? float(sqrt(sq / double(E)) + 1e-6) : NAN;
+      } else {
+        // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
+        if (lane == 0) *p.l_aux = okb ? float(double(E) * aux / (S * S)) : NAN;
+      }
+    }
+  }
+}
+
+unsigned int next_barrier_slot() {
+  static std::atomic<unsigned int> n{0};
+  return n.fetch_add(1u, std::memory_order_relaxed) % kGateBarrierSlots;
+}
+
+}  // namespace
+
+cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
+  if (a.S <= 0) return cudaErrorNotSupported;
+  const int nsm = num_sms();
+  int64_t tm = (a.S + nsm - 1) / nsm;
+  tm = (tm + 7) & ~int64_t(7);
+  if (tm < 16) tm = 16;
+  if (tm > kGrMaxTile) return cudaErrorNotSupported;  // more tokens than one wave of tiles
+  GrParams p{};
+  p.S = a.S; p.d = a.d; p.E = a.E; p.k = a.k;
+  p.TM = int(tm);
+  p.ntiles = int((a.S + tm - 1) / tm);
+  p.E_pad = (a.E + 15) / 16 * 16;
+  uint32_t cols = 32;
+  while (int(cols) < p.E_pad) cols <<= 1;
+  p.tmem_cols = cols;
+  p.nbox = MOE_GATE_BOXES;
+  p.nk64 = (a.d + 63) / 64;
+  p.nk = (p.nk64 + p.nbox - 1) / p.nbox;
+  p.stage_bytes = uint32_t(p.nbox) * (kXBoxBytes + uint32_t(p.E_pad) * 128);
+  constexpr size_t kSmemLimit = 232448;
+  const size_t fixed = 1024 + sizeof(GrCtl);
+  int nst = int((kSmemLimit - fixed) / p.stage_bytes);
+  if (nst > kGrMaxStages) nst = kGrMaxStages;
+  if (nst > p.nk) nst = p.nk;
+  if (nst < 1) return cudaErrorNotSupported;
+  p.nstages = nst;
+  p.hist_pitch = (a.k * a.E + 3) & ~3;
+  p.psum_pitch = (a.E + 3) & ~3;
+  // the ring also holds the epilogue's transpose tiles and phase B's
+  // reduction scratch
+  size_t ring = size_t(nst) * p.stage_bytes;
+  const int rg_aux = std::max(1, kGrThreads / (p.psum_pitch >> 2));
+  const size_t need = std::max({size_t(4) * kStgFloats * 4, size_t(2) * kGrThreads * 16,
+                                size_t(rg_aux) * p.psum_pitch * 8});
+  if (ring < need) return cudaErrorNotSupported;
+  const size_t smem = fixed + ring;
+  if (smem > kSmemLimit) return cudaErrorNotSupported;
+  const size_t ws_need = size_t(p.ntiles) * (p.hist_pitch + p.psum_pitch) * 4;
+  if (ws_need > a.ws_bytes) return cudaErrorNotSupported;
+  p.hist = static_cast<int32_t *>(a.ws);
+  p.psum = reinterpret_cast<float *>(static_cast<char *>(a.ws) +
+                                     size_t(p.ntiles) * p.hist_pitch * 4);
+  p.idesc = ptx::idesc_bf16(128, p.E_pad, 0, 0);
+  p.cap = a.cap;
+  p.rows_alloc = a.rows_alloc;
+  p.logit_bias = a.logit_bias; p.bias_ld = a.bias_ld; p.inv_temp = a.inv_temp;
+  p.aux_type = a.aux_type;
+  p.logits = a.logits; p.probs = a.probs; p.idx = a.idx; p.w = a.w; p.slot = a.slot;
+  p.routed = a.routed; p.kept = a.kept; p.offsets = a.offsets; p.row_src = a.row_src;
+  p.l_aux = a.l_aux; p.err = a.err;
+  p.barrier_slot = next_barrier_slot();
+
+  CUtensorMap tx, tw;
+  if (!make_bf16_map(&tx, a.x, uint64_t(a.d), uint64_t(a.S), 64, uint32_t(p.TM)))
+    return cudaErrorInvalidValue;
+  if (!make_bf16_map(&tw, a.w_gate, uint64_t(a.d), uint64_t(a.E), 64, uint32_t(p.E_pad)))
+    return cudaErrorInvalidValue;
+  static PerDevice<int> smem_raised;
+  int unused = 0;
+  if (const cudaError_t e = smem_raised.get(&unused, [](int &) {
+        return cudaFuncSetAttribute(gate_route_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemLimit));
+      }); e != cudaSuccess)
+    return e;
+  // cooperative: every CTA resident at once (the grid barrier needs it);
+  // programmatic serialization: overlaps the launch with the previous kernel
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(unsigned(p.ntiles));
+  lc.blockDim = dim3(kGrThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&lc, gate_route_kernel, tx, tw, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // a rejected configuration is not sticky
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, gate_route_kernel, tx, tw, p);
+  }
+  return e;
+}
+
+}  // namespace moe

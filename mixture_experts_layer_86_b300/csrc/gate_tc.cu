@@ -320,37 +320,6 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn gate_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-bool gate_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
-  EncodeTiledFn fn = gate_encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st) {
@@ -360,8 +329,8 @@ cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st) {
   uint32_t cols = 32;
   while (int(cols) < E_pad) cols <<= 1;
   CUtensorMap tx, tw;
-  if (!gate_map(&tx, a.x, uint64_t(a.d), uint64_t(a.S), GBK, GBM)) return cudaErrorInvalidValue;
-  if (!gate_map(&tw, a.w_gate, uint64_t(a.d), uint64_t(a.E), GBK, uint32_t(E_pad)))
+  if (!make_bf16_map(&tx, a.x, uint64_t(a.d), uint64_t(a.S), GBK, GBM)) return cudaErrorInvalidValue;
+  if (!make_bf16_map(&tw, a.w_gate, uint64_t(a.d), uint64_t(a.E), GBK, uint32_t(E_pad)))
     return cudaErrorInvalidValue;
   // As many ring stages as fit (at most kMaxGateStages, at most one per K
   // block): the stage is one CTA per SM, so the bytes it keeps in flight

@@ -377,6 +377,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 //   even CTA    warp 1: the pair's MMAs; commits are multicast to the
 //               `empty` / `tfull` barriers of both CTAs
 // TMEM is allocated and freed by warp 1 of both CTAs together.
+//
+// Gather form (kGather, the W1 GEMM of the forward with the dispatch fused
+// in, MoE explainer §3.1: dispatch, compute and combine in one pass without
+// the flattened copy): the token operand is not read from an expert-major
+// copy x_disp but straight from the token matrix x, row r of the group
+// being token row_src[r] / k.  Four more warps per CTA gather this CTA's
+// half of the token tile with 16-byte cp.async copies into the same
+// 128-byte-swizzled layout the TMA would write (rows past the group are
+// zero), wait for them, fence them for the tensor cores and arrive on the
+// even CTA's `full` barrier, which then counts the weight bytes of both
+// CTAs' TMA loads and the gather warps of both CTAs.
 constexpr int kPairKH = 2;                  // 64-wide K halves per stage
 constexpr int kPairBK = 64 * kPairKH;       // K per stage
 constexpr int kPairStages = 6 / kPairKH;
@@ -400,18 +411,22 @@ struct __align__(8) PairCtl {
 // epilogue keeps up with tiles whose K loop is short (d = 512 or 1024)
 constexpr int kPairEpiWarps = 8;
 constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
+constexpr int kPairGatherWarps = 4;
+constexpr int kPairThreadsGather = kPairThreads + 32 * kPairGatherWarps;
 constexpr size_t kPairSmemBytes = 1024 + kPairStages * (kPairABytes + kPairBBytes) +
                                   kPairEpiWarps * kStageBytesPerWarp + sizeof(PairCtl);
 
-template <bool kWMN>
-__global__ void __launch_bounds__(kPairThreads, 1)
+template <bool kWMN, bool kGather>
+__global__ void __launch_bounds__(kGather ? kPairThreadsGather : kPairThreads, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX,
                     const int32_t *__restrict__ offsets, int64_t dense_rows, int G, int N,
                     int K,
                     const __nv_bfloat16 *__restrict__ bias, int act,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
-                    const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err) {
+                    const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err,
+                    const __nv_bfloat16 *__restrict__ xg, const int32_t *__restrict__ row_src,
+                    int kch) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -430,7 +445,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      // the producer's arrive (+ the gather warps of both CTAs)
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), kGather ? 1 + 2 * kPairGatherWarps : 1);
       ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -489,7 +505,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
           const uint32_t fb_local = ptx::smem_addr(&ctl.full[stage]);
           const uint32_t fb = ptx::mapa_shared(fb_local, 0);
           if (rank == 0)
-            ptx::mbar_arrive_expect_tx(fb_local, 2 * (kPairABytes + kPairBBytes));
+            ptx::mbar_arrive_expect_tx(fb_local,
+                                       kGather ? 2 * kPairABytes : 2 * (kPairABytes + kPairBBytes));
 #pragma unroll
           for (int h = 0; h < kPairKH; ++h) {
             const int k0 = kb * kPairBK + h * 64;
@@ -502,8 +519,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                 ptx::tma_load_2d_pair(ptx::smem_addr(a + j * (64 * 128)), &tmW, fb, frow + j * 64,
                                       tc.g * K + k0);
             }
-            ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes + h * kHalfBytes), &tmX,
-                                  fb, k0, xrow);
+            if (!kGather)
+              ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes + h * kHalfBytes),
+                                    &tmX, fb, k0, xrow);
           }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -573,6 +591,76 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       ptx::mma_commit_pair(ptx::smem_addr(&ctl.drain));
       if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
         record_error(err, kErrGemmDrain);
+    }
+  } else if (kGather && warp >= 2 + kPairEpiWarps) {
+    // ------------------- token rows gathered from x (the fused dispatch)
+    // this warp's 32 rows of the CTA's half of the token tile, 4 rows per
+    // pass: 8 lanes x 16 bytes = one 64-wide K half of a row
+    const int gw = warp - (2 + kPairEpiWarps);
+    const int c16 = lane & 7, rsub = lane >> 3;
+    const uint32_t full_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.full[0]), 0);
+    int stage = 0, pend = -1;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = cid; t < total && ok; t += ncl) {
+      const TileCoord tc = tile_coord(ctl, G, nf, t);
+      const int half = ((tc.ntok + 15) & ~15) >> 1;   // token rows per CTA in the MMA
+      const int first = tc.tt * kTok + int(rank) * half;
+      const int nvalid = tc.ntok - int(rank) * half;  // rows of the group in this half
+      int64_t src[8];                                  // element offset of each row in x
+#pragma unroll
+      for (int ps = 0; ps < 8; ++ps) {
+        const int r = gw * 32 + ps * 4 + rsub;
+        src[ps] = (r < half && r < nvalid) ? int64_t(row_src[tc.row0 + first + r] / kch) * K : -1;
+      }
+      for (int kb = 0; kb < nk; ++kb) {
+        bool got = true;
+        if (lane == 0)
+          got = ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort,
+                                       kWaitLimitNs);
+        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          if (lane == 0) {
+            record_error(err, kErrGemmGather | uint32_t(t & 0xffffff));
+            *abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        uint8_t *sb = sB + stage * kPairBBytes;
+#pragma unroll
+        for (int ps = 0; ps < 8; ++ps) {
+          const int r = gw * 32 + ps * 4 + rsub;
+          if (r >= half) continue;  // the MMA reads `half` rows of this CTA
+#pragma unroll
+          for (int h = 0; h < kPairKH; ++h) {
+            const int col = kb * kPairBK + h * 64 + c16 * 8;
+            const bool in = src[ps] >= 0 && col < K;
+            ptx::cp_async_16(
+                ptx::smem_addr(sb + h * kHalfBytes + r * 128 + ((c16 ^ (r & 7)) << 4)),
+                in ? static_cast<const void *>(xg + src[ps] + col) : static_cast<const void *>(xg),
+                in ? 16u : 0u);
+          }
+        }
+        ptx::cp_async_commit();
+        if (pend >= 0) {  // the previous stage's copies have landed: hand it to the MMA
+          ptx::cp_async_wait<1>();
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend) * 8u);
+        }
+        pend = stage;
+        if (++stage == kPairStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ptx::cp_async_wait<0>();
+    if (pend >= 0) {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend) * 8u);
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
@@ -934,6 +1022,338 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
+// --------------------------------------- K-grouped weight gradient, CTA pairs
+// The same K-grouped product with tcgen05.mma.cta_group::2: a 2-CTA cluster
+// computes a 256 (M) x 256 (N) tile of C_g.  Each CTA loads its own 128
+// columns of A (the M half whose rows of D live in its TMEM) and 128 of the
+// 256 columns of B (tcgen05 splits B's N between the pair), 128 K rows per
+// stage: 64 KB per CTA per stage instead of the 96 KB that a single-CTA
+// 128 x 256 tile needs for the same work.
+//   both CTAs  warp 0: TMA loads of this CTA's halves into its ring, landing
+//              on its own `full` barrier; warp 10: waits `full`, zeroes the
+//              rows past the group (they may hold the next group's rows or
+//              unwritten memory), sums A's columns over the group's rows
+//              when the tile is the first N tile (the bias gradient
+//              db_g = sum over rows of A), and arrives on the even CTA's
+//              `ready` barrier; warps 2..9: epilogue of this CTA's 128 rows
+//   even CTA   warp 1: waits `ready` (both CTAs' arrivals), issues the pair
+//              MMAs; commits are multicast to both CTAs' `empty` / `tfull`.
+constexpr int kWpBK = 128;                   // K rows per stage (two 64-row halves)
+constexpr int kWpStages = 3;
+constexpr uint32_t kWpBoxBytes = 64 * 64 * 2;               // 64 cols x 64 rows, 8 KB
+constexpr uint32_t kWpOpBytes = 4 * kWpBoxBytes;            // one operand half per stage, 32 KB
+constexpr int kWpEpiWarps = 8;
+constexpr int kWpFixupWarp = 2 + kWpEpiWarps;
+constexpr int kWpThreads = 32 * (kWpFixupWarp + 1);
+
+struct __align__(8) WpCtl {
+  uint64_t full[kWpStages];
+  uint64_t ready[kWpStages];
+  uint64_t empty[kWpStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kWpSmemBytes = 1024 + kWpStages * 2 * kWpOpBytes + sizeof(WpCtl);
+
+// Stage layout of one operand half: [k half 0: cols 0-63, cols 64-127]
+// [k half 1: cols 0-63, cols 64-127], each box 64 K rows of 128 B
+// (MN-major, 128-byte swizzle).
+__global__ void __launch_bounds__(kWpThreads, 1)
+tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const int32_t *__restrict__ offsets, int G, int M, int N,
+                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ colsum,
+                     unsigned int *err) {
+  griddep_begin();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kWpStages * kWpOpBytes;
+  WpCtl &ctl = *reinterpret_cast<WpCtl *>(smem + kWpStages * 2 * kWpOpBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int mt = (M + 255) / 256, nt = (N + 255) / 256;
+  const int total = G * mt * nt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWpStages; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 2);  // the fixup warp of each CTA
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 2 * kWpEpiWarps);  // both CTAs
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
+    ctl.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  block_sync();
+  ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  volatile int *abort = &ctl.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        int g, m, n;
+        wg_tile(t, mt, nt, g, m, n);
+        const int r0 = offsets[g], rows = offsets[g + 1] - r0;
+        const int nk = (rows + kWpBK - 1) / kWpBK;
+        const int acol = m * 256 + int(rank) * 128, bcol = n * 256 + int(rank) * 128;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort,
+                                      kWaitLimitNs)) {
+            record_error(err, kErrWgradProducer | uint32_t(t & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, 2 * kWpOpBytes);
+          const int row = r0 + kb * kWpBK;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
+              ptx::tma_load_2d(ptx::smem_addr(sA + off), &tmA, fb, acol + j * 64, row + h * 64);
+              ptx::tma_load_2d(ptx::smem_addr(sB + off), &tmB, fb, bcol + j * 64, row + h * 64);
+            }
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kWpStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every stage filled here has been read by the pair's MMAs before the
+      // CTA moves on (or, after a give-up, at least its copies have landed)
+      for (int s = 0; s < kWpStages; ++s)
+        if (armed & (1u << s)) {
+          if (ok)
+            ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[s]), (armed_phase >> s) & 1u,
+                                   nullptr, kWaitLimitNs);
+          else
+            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+                           kWaitLimitNs / 4);
+        }
+    }
+  } else if (warp == kWpFixupWarp) {
+    // ------------ fixup: rows past the group, bias-gradient column sums
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const uint32_t ready_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.ready[0]), 0);
+    // this lane's 4 columns of A (of the CTA's 128): box j, 16-byte chunk, offset
+    const int cj = lane >> 4, cchunk = (lane & 15) >> 1, csub = (lane & 1) * 8;
+    for (int t = cid; t < total && ok; t += ncl) {
+      int g, m, n;
+      wg_tile(t, mt, nt, g, m, n);
+      const int rows = offsets[g + 1] - offsets[g];
+      const int nk = (rows + kWpBK - 1) / kWpBK;
+      const bool sum = colsum != nullptr && n == 0;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int kb = 0; kb < nk; ++kb) {
+        bool got = true;
+        if (lane == 0)
+          got = ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs);
+        got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          if (lane == 0) {
+            record_error(err, kErrWgradFixup | uint32_t(t & 0xffffff));
+            *abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        const int valid = rows - kb * kWpBK;
+        if (valid < kWpBK) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int vr = max(0, min(64, valid - h * 64));  // valid rows of this K half
+            const int nbytes = (64 - vr) * 128;              // contiguous tail of each box
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes + vr * 128;
+              for (int i = lane * 16; i < nbytes; i += 32 * 16) {
+                *reinterpret_cast<uint4 *>(sA + off + i) = z;
+                *reinterpret_cast<uint4 *>(sB + off + i) = z;
+              }
+            }
+          }
+          ptx::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (sum) {
+          // rows past the group are zero now: add all 128 rows, in order
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t *box = sA + stage * kWpOpBytes + (h * 2 + cj) * kWpBoxBytes;
+#pragma unroll 4
+            for (int kr = 0; kr < 64; ++kr) {
+              const uint2 v = *reinterpret_cast<const uint2 *>(
+                  box + kr * 128 + ((cchunk ^ (kr & 7)) << 4) + csub);
+              acc[0] += __uint_as_float(v.x << 16);
+              acc[1] += __uint_as_float(v.x & 0xffff0000u);
+              acc[2] += __uint_as_float(v.y << 16);
+              acc[3] += __uint_as_float(v.y & 0xffff0000u);
+            }
+          }
+          __syncwarp();
+        }
+        ptx::fence_proxy_async_smem();  // this CTA's stage is complete for the MMA's reads
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote(ready_leader + uint32_t(stage) * 8u);
+        if (++stage == kWpStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (sum && ok) {
+        const int col = m * 256 + int(rank) * 128 + cj * 64 + cchunk * 8 + (csub >> 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (col + c < M) colsum[int64_t(g) * M + col + c] = __float2bfloat16_rn(acc[c]);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(256, 256, 1, 1);
+      const uint64_t a_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sA), kWpBoxBytes, 1024);
+      const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), kWpBoxBytes, 1024);
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl, ++it) {
+        int g, m, n;
+        wg_tile(t, mt, nt, g, m, n);
+        const int rows = offsets[g + 1] - offsets[g];
+        const int nk = (rows + kWpBK - 1) / kWpBK;
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort,
+                                    kWaitLimitNs)) {
+          record_error(err, kErrWgradMma | 0x800000u | uint32_t(t & 0x7fffff));
+          *abort = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * 256);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.ready[stage]), phase, abort,
+                                      kWaitLimitNs)) {
+            record_error(err, kErrWgradMma | uint32_t(t & 0x7fffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t so = stage * kWpOpBytes;
+#pragma unroll
+          for (int kk = 0; kk < kWpBK / 16; ++kk) {
+            const uint32_t off = so + uint32_t(kk >> 2) * (2 * kWpBoxBytes) + uint32_t(kk & 3) * (16 * 128);
+            ptx::mma_bf16_pair(d_tmem, ptx::sdesc_add(a_desc0, off), ptx::sdesc_add(b_desc0, off),
+                               idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_mc(ptx::smem_addr(&ctl.empty[stage]), kPairMask);
+          if (++stage == kWpStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) ptx::mma_commit_pair_mc(ptx::smem_addr(&ctl.tfull[acc]), kPairMask);
+      }
+      ptx::mma_commit_pair(ptx::smem_addr(&ctl.drain));
+      if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
+        record_error(err, kErrGemmDrain);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;             // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;   // which alternate 32-column chunks
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.tempty[0]), 0);
+    int it = 0;
+    for (int t = cid; t < total; t += ncl, ++it) {
+      int g, m, n;
+      wg_tile(t, mt, nt, g, m, n);
+      const bool empty_group = offsets[g + 1] == offsets[g];
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort,
+                                  kWaitLimitNs)) {
+        record_error(err, kErrWgradEpilogue | uint32_t(t & 0xffffff));
+        *abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const int row = m * 256 + int(rank) * 128 + r_in_tile;
+      const bool valid = row < M;
+      __nv_bfloat16 *crow = C + (int64_t(g) * M + row) * N;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * 256);
+#pragma unroll 1
+      for (int c = half; c < 256 / 32; c += 2) {
+        uint32_t raw[32];
+        if (!empty_group) {
+          ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) raw[i] = 0u;
+        }
+        const int n0 = n * 256 + c * 32;
+        if (!valid || n0 >= N) continue;
+#pragma unroll
+        for (int v8 = 0; v8 < 4; ++v8) {
+          const int col = n0 + v8 * 8;
+          if (col >= N) break;
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
+          *reinterpret_cast<uint4 *>(crow + col) = pack_bf16x8(x);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(tempty_leader + uint32_t(acc) * 8u);
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  block_sync();
+  ptx::cluster_sync();  // the pair's MMAs, epilogues and remote arrivals are done
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ----------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -941,22 +1361,22 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static EncodeTiledFn fn = [] {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a
-// box of [box_outer, box_inner] elements and 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
+}  // namespace
+
+bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                   uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -968,14 +1388,49 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
   if (g.G <= 0) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, g.A, uint64_t(g.M), uint64_t(g.rows_alloc), 64, BK) ||
-      !make_map(&tb, g.B, uint64_t(g.N), uint64_t(g.rows_alloc), 64, BK))
+  if (!make_bf16_map(&ta, g.A, uint64_t(g.M), uint64_t(g.rows_alloc), 64, BK) ||
+      !make_bf16_map(&tb, g.B, uint64_t(g.N), uint64_t(g.rows_alloc), 64, BK))
     return cudaErrorInvalidValue;
+  const int sms = num_sms();
+  if (sms >= 2) {
+    // CTA pairs: 256 x 256 tiles, one M half of A and one N half of B per CTA
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.blockDim = dim3(kWpThreads);
+    lc.dynamicSmemBytes = kWpSmemBytes;
+    lc.stream = st;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    static PerDevice<int> resident_pairs;
+    int npairs = 0;
+    cudaError_t e = resident_pairs.get(&npairs, [&](int &v) {
+      cudaError_t r = cudaFuncSetAttribute(tc_wgrad_pair_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(kWpSmemBytes));
+      if (r != cudaSuccess) return r;
+      lc.gridDim = dim3(sms & ~1);
+      int ncl = 0;
+      r = cudaOccupancyMaxActiveClusters(&ncl, tc_wgrad_pair_kernel, &lc);
+      if (r != cudaSuccess) return r;
+      if (ncl < 1) return cudaErrorInvalidConfiguration;
+      v = ncl < sms / 2 ? ncl : sms / 2;
+      return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
+    const int tiles = g.G * ((g.M + 255) / 256) * ((g.N + 255) / 256);
+    lc.gridDim = dim3(2 * (tiles < npairs ? tiles : npairs));
+    return cudaLaunchKernelEx(&lc, tc_wgrad_pair_kernel, ta, tb, g.offsets, g.G, g.M, g.N,
+                              static_cast<__nv_bfloat16 *>(g.C),
+                              static_cast<__nv_bfloat16 *>(g.colsum), g.err);
+  }
+  if (g.colsum) return cudaErrorNotSupported;  // the single-CTA kernel has no column sums
   static PerDevice<int> smem_raised;
   int unused = 0;
   if (const cudaError_t e = smem_raised.get(&unused, [](int &) {
@@ -992,37 +1447,43 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
   if (g.G <= 0 || g.G > kMaxGroups) return cudaErrorInvalidValue;
   CUtensorMap tw, tx;
-  if (!make_map(&tx, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, kTok))
+  if (!make_bf16_map(&tx, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, kTok))
     return cudaErrorInvalidValue;
   bool okw;
   if (g.b_kmajor)
-    okw = make_map(&tw, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, kFeat);
+    okw = make_bf16_map(&tw, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, kFeat);
   else
-    okw = make_map(&tw, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
+    okw = make_bf16_map(&tw, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
   if (!okw) return cudaErrorInvalidValue;
 
   const int sms = num_sms();
   if (sms >= 2) {
     // CTA pairs: this CTA's weight rows (128) and half of the token tile
     CUtensorMap txp;
-    if (!make_map(&txp, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, 128))
+    if (!make_bf16_map(&txp, g.A, uint64_t(g.K), uint64_t(g.rows_alloc), BK, 128))
       return cudaErrorInvalidValue;
-    const int which = g.b_kmajor ? 0 : 1;
-    auto kern = g.b_kmajor ? tc_gemm_pair_kernel<false> : tc_gemm_pair_kernel<true>;
+    // 0: weights K-major, 1: weights MN-major (data gradient), 2: the gather
+    // form (weights K-major, token rows read from x through row_src)
+    const bool gather = g.row_src != nullptr;
+    if (gather && !g.b_kmajor) return cudaErrorInvalidValue;
+    const int which = gather ? 2 : (g.b_kmajor ? 0 : 1);
+    auto kern = gather ? tc_gemm_pair_kernel<false, true>
+                       : (g.b_kmajor ? tc_gemm_pair_kernel<false, false>
+                                     : tc_gemm_pair_kernel<true, false>);
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    lc.blockDim = dim3(kPairThreads);
+    lc.blockDim = dim3(gather ? kPairThreadsGather : kPairThreads);
     lc.dynamicSmemBytes = kPairSmemBytes;
     lc.stream = st;
     lc.attrs = attr;
     lc.numAttrs = 1;
     // persistent grid: as many pairs as can be resident at once (the
     // shared-memory limit is raised and the occupancy asked once per device)
-    static PerDevice<int> resident_pairs[2];
+    static PerDevice<int> resident_pairs[3];
     int npairs = 0;
     const cudaError_t e = resident_pairs[which].get(&npairs, [&](int &v) {
       cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1042,8 +1503,10 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
                               static_cast<const __nv_bfloat16 *>(g.bias), g.act,
                               static_cast<__nv_bfloat16 *>(g.C),
                               static_cast<__nv_bfloat16 *>(g.pre),
-                              static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err);
+                              static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err,
+                              static_cast<const __nv_bfloat16 *>(g.A), g.row_src, g.k_choices);
   }
+  if (g.row_src) return cudaErrorNotSupported;  // the gather form needs CTA pairs
   static PerDevice<int> smem_raised[2];
   const int which = g.b_kmajor ? 0 : 1;
   auto kern = g.b_kmajor ? tc_gemm_kernel<false> : tc_gemm_kernel<true>;

@@ -2,6 +2,7 @@
 // the kernel translation units and the C ABI (api.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -48,6 +49,13 @@ class PerDevice {
 // Tokens per gate/routing CTA; the slot scan works on per-CTA histograms.
 constexpr int kRouteTokensPerCta = 128;
 
+// 2-D bf16 TMA tensor map over a row-major [outer, inner] matrix with a box
+// of [box_outer, box_inner] elements, 128-byte swizzle and zero fill out of
+// bounds.  False when the driver entry point is missing or the encoding is
+// rejected (misaligned base or stride, box too large).
+bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                   uint32_t box_inner, uint32_t box_outer);
+
 // ---------------------------------------------------------------- routing
 struct RouteArgs {
   const float *logits;  // [S,E] fp32 (bias included)
@@ -93,6 +101,33 @@ struct GateTcArgs {
 };
 cudaError_t launch_gate_tc(const GateTcArgs &a, cudaStream_t st);
 
+// Single-launch bf16 gate: the fused gate above plus the slot scan and
+// assignment, counts, offsets and l_aux, with a grid-wide barrier between
+// the two halves.  Returns cudaErrorNotSupported (enqueueing nothing) when
+// the batch does not fit one wave of tiles of at most 128 tokens per SM or
+// the workspace is too small; the caller then takes the three-launch path.
+struct GateRouteArgs {
+  const void *x, *w_gate;   // bf16 [S,d], [E,d]
+  int64_t S;
+  int d, E, k;
+  int64_t cap;              // -1: no capacity limit
+  int64_t rows_alloc;       // rows of the expert-major buffers (moe_max_rows)
+  const float *logit_bias;  // [E] (bias_ld 0) or [S,E] (bias_ld E), or null
+  int bias_ld;
+  float inv_temp;
+  int aux_type;
+  float *logits, *probs;    // [S,E] or null
+  int32_t *idx;
+  float *w;
+  int32_t *slot;
+  int32_t *routed, *kept, *offsets, *row_src;
+  float *l_aux;
+  void *ws;                 // per-tile counts and probability sums
+  size_t ws_bytes;
+  unsigned int *err;
+};
+cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st);
+
 // ------------------------------------------------------ SIMT grouped GEMM
 // C(m,n) = epilogue( sum_k A(m,k) * B(n,k) ) with arbitrary element strides.
 //  mode 0: one GEMM of M x N x K.
@@ -128,6 +163,10 @@ cudaError_t launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
 // (b_kmajor) or columns of a [G*K, N] (!b_kmajor) bf16 matrix.
 // Epilogue: + bias[g*N + n] (bf16, nullable), store pre (bf16, nullable),
 // act (>= 0), times act'(grad_src[r, n]) when grad_src is set; C bf16.
+// Gather form (row_src set): A is the token matrix x [rows_alloc = S, K]
+// and row r of the grouped operand is token row_src[r] / k_choices of it
+// (the dispatch copy fused into the GEMM); C, pre and the groups keep the
+// expert-major row order.  Needs b_kmajor and CTA pairs.
 struct TcGemm {
   const void *A; int64_t rows_alloc;   // rows of the A/C allocations
   const void *B; bool b_kmajor;
@@ -139,17 +178,22 @@ struct TcGemm {
   void *pre;
   const void *grad_src; int dact;
   unsigned int *err;
+  const int32_t *row_src;  // gather form: [rows] s*k+j of each row, else null
+  int k_choices;
 };
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 
 // K-grouped bf16 weight-gradient GEMM on the tensor cores:
 //   C_g[m, n] = sum over rows r of group g of A[r, m] * B[r, n]
 // A: [rows, M] bf16, B: [rows, N] bf16 (both row-major), C: [G, M, N] bf16.
+// colsum (nullable): [G, M] bf16, the column sums of A over each group's
+// rows (the bias gradient that goes with the weight gradient).
 struct TcWgrad {
   const void *A; const void *B; int64_t rows_alloc;
   void *C;
   int M, N, G;
   const int32_t *offsets;
+  void *colsum;
   unsigned int *err;
 };
 cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);

@@ -16,8 +16,11 @@ def torch_dtype(cfg: N.MoeConfig) -> torch.dtype:
     return torch.float32 if cfg.dtype == N.MOE_F32 else torch.bfloat16
 
 
-def alloc_buffers(cfg: N.MoeConfig, device, training: bool = False) -> dict:
-    """Device buffers of one forward pass, sized from the config alone."""
+def alloc_buffers(cfg: N.MoeConfig, device, training: bool = False,
+                  fused_dispatch: bool = False) -> dict:
+    """Device buffers of one forward pass, sized from the config alone.  With
+    fused_dispatch (bf16 inference) there is no x_disp: moe_forward then reads
+    the experts' token rows straight from x inside the first expert GEMM."""
     S, E, k = cfg.num_tokens, cfg.num_experts, cfg.k
     d, f = cfg.hidden_size, cfg.ffn_size
     R = N.moe_max_rows(cfg)
@@ -35,7 +38,7 @@ def alloc_buffers(cfg: N.MoeConfig, device, training: bool = False) -> dict:
         "expert_offsets": torch.empty((E + 1,), **i32),
         "row_src": torch.empty((max(R, 1),), **i32),
         "l_aux": torch.empty((1,), **f32),
-        "x_disp": torch.empty((max(R, 1), d), dtype=dt, device=device),
+        "x_disp": None if fused_dispatch else torch.empty((max(R, 1), d), dtype=dt, device=device),
         "h_pre": torch.empty((max(R, 1), f), dtype=dt, device=device) if training else None,
         "h": torch.empty((max(R, 1), f), dtype=dt, device=device),
         "out_disp": torch.empty((max(R, 1), d), dtype=dt, device=device),
@@ -48,10 +51,10 @@ def alloc_workspace(cfg: N.MoeConfig, device, for_backward: bool = False) -> tor
 
 
 def forward(cfg, x, w_gate, logit_bias, w1, b1, w2, b2, bufs=None, workspace=None,
-            y=None, training=False, stream=None):
+            y=None, training=False, stream=None, fused_dispatch=False):
     dev = x.device
     if bufs is None:
-        bufs = alloc_buffers(cfg, dev, training)
+        bufs = alloc_buffers(cfg, dev, training, fused_dispatch=fused_dispatch and not training)
     if workspace is None:
         workspace = alloc_workspace(cfg, dev)
     if y is None:

@@ -8,7 +8,7 @@ import torch
 
 from _harness import DEV, GpuRun, WORKLOADS, assert_close, check_routing_equal, f64, oracle_cfg
 from mixture_experts_layer_86_b300 import _native as N
-from mixture_experts_layer_86_b300.inputs import make_inputs
+from mixture_experts_layer_86_b300.inputs import Workload, make_inputs
 from oracle import moe_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +42,19 @@ def test_backward_parity(name, S):
     ref, gref = _oracle_grads(run)
     check_routing_equal(run, ref)
     print(name, S, _check_all(run, ref, gref))
+
+
+def test_backward_odd_widths():
+    """d = 96 and f = 160 are multiples of 8 but not of the 64-wide TMA boxes
+    or the 256-wide weight-gradient tiles: partial boxes on both sides and
+    bias-gradient columns past the end of the tile."""
+    wl = Workload("odd_widths", 700, 96, 160, 6, 2, 1.25, 4, True, "gelu_tanh", "bf16",
+                  seed=13, bias_std=0.1, aux_loss_weight=0.01, backward=True)
+    run = GpuRun(wl, training=True)
+    run.backward()
+    ref, gref = _oracle_grads(run)
+    check_routing_equal(run, ref)
+    print("odd widths", _check_all(run, ref, gref))
 
 
 def test_backward_empty_expert_gets_zero_gradient():

@@ -105,10 +105,11 @@ def test_route_hand_worked_case():
 
 @pytest.mark.parametrize("S", [18000, 20000])
 def test_gate_routing_beyond_one_wave(S):
-    """The bf16 gate at d=2048 fits one 128-token CTA per SM: 18000 tokens
-    (141 CTAs, ragged last CTA) run in one wave on a 148-SM B300, 20000
-    tokens (157 CTAs) need a second.  Routing must match the oracle on the
-    GPU's own logits either way."""
+    """The single-launch bf16 gate takes one tile of at most 128 tokens per
+    SM: 18000 tokens are 141 tiles of 128 (ragged last tile) on a 148-SM
+    B300; 20000 tokens need more than one tile per SM, so the gate runs as
+    three launches (fused gate kernel, slot scan, slot assignment).  Routing
+    must match the oracle on the GPU's own logits either way."""
     wl = WORKLOADS["e8_bf16"].scaled(S)
     wl = type(wl)(**{**wl.__dict__, "hidden_size": 2048, "ffn_size": 64, "name": f"gate_S{S}"})
     run = GpuRun(wl, training=True)
