@@ -92,11 +92,17 @@ def workload_desc(wl) -> str:
             + (f" skew={wl.skew}" if wl.skew else ""))
 
 
-def forward_launches(wl) -> int:
-    """Kernels one forward pass launches: the bf16 gate (fused gate kernel,
-    slot scan, slot assignment) or the fp32 gate (router GEMM, top-k, scan,
-    assignment), dispatch, the two expert GEMMs and the combine."""
-    return (3 if wl.dtype == "bf16" else 4) + 1 + 2 + 1
+def forward_launches(wl, fused: bool, num_sms: int) -> int:
+    """Kernels one forward pass launches: the gate -- one launch for bf16
+    batches of at most 128 tokens per SM, else three (fused gate kernel, slot
+    scan, slot assignment); four for fp32 (router GEMM, top-k, scan,
+    assignment) -- the dispatch copy unless it is fused into the first expert
+    GEMM, the two expert GEMMs and the combine."""
+    if wl.dtype == "bf16":
+        gate = 1 if wl.num_tokens <= 128 * num_sms else 3
+    else:
+        gate = 4
+    return gate + (0 if fused else 1) + 2 + 1
 
 
 # ------------------------------------------------------------------ clocks
@@ -218,10 +224,13 @@ STAGES = ("gate", "dispatch", "expert_ffn", "combine")
 
 class LayerRun:
     """Device state of one workload (inputs, buffers, workspaces) and its
-    stage calls through the C ABI.  The forward runs the four stage entry
-    points, the kernels moe_forward launches in its order."""
+    stage calls through the C ABI.  The forward runs the stage entry points,
+    the kernels moe_forward launches in its order: for a bf16 forward without
+    a backward, the dispatch is fused into the first expert GEMM
+    (moe_expert_ffn_gather, no x_disp copy), else moe_dispatch then
+    moe_expert_ffn."""
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, fused=None):
         import torch
 
         from mixture_experts_layer_86_b300 import _native as N
@@ -233,7 +242,11 @@ class LayerRun:
         self.inp_cpu = make_inputs(wl)
         self.d = self.inp_cpu.to(dev)
         self.train = wl.backward
-        self.bufs = L.alloc_buffers(self.cfg, dev, training=self.train)
+        self.fused = (wl.dtype == "bf16" and not self.train) if fused is None else fused
+        self.names = (("gate", "expert_ffn", "combine") if self.fused else STAGES) + \
+            (("backward",) if self.train else ())
+        self.bufs = L.alloc_buffers(self.cfg, dev, training=self.train,
+                                    fused_dispatch=self.fused)
         self.bufs["logits"] = None      # optional output of the gate; nothing downstream reads it
         self.ws = L.alloc_workspace(self.cfg, dev)
         self.y = torch.empty_like(self.d.x)
@@ -252,6 +265,9 @@ class LayerRun:
                             b["expert_offsets"], b["row_src"], b["l_aux"], self.ws, st)
         elif name == "dispatch":
             N.moe_dispatch(c, d.x, b["topk_idx"], b["slot"], b["expert_offsets"], b["x_disp"], st)
+        elif name == "expert_ffn" and self.fused:
+            N.moe_expert_ffn_gather(c, d.x, b["row_src"], b["expert_offsets"], d.w1, d.b1, d.w2,
+                                    d.b2, b["h_pre"], b["h"], b["out_disp"], st)
         elif name == "expert_ffn":
             N.moe_expert_ffn(c, b["x_disp"], b["expert_offsets"], d.w1, d.b1, d.w2, d.b2,
                              b["h_pre"], b["h"], b["out_disp"], st)
@@ -266,9 +282,8 @@ class LayerRun:
     def step(self, st, ev=None, marks=()):
         """One step; ev[i] is recorded just before the i-th stage named in
         `marks` ("end": after the last stage)."""
-        names = STAGES + (("backward",) if self.train else ())
         j = 0
-        for name in names + ("end",):
+        for name in self.names + ("end",):
             if ev is not None and name in marks:
                 ev[j].record(st)
                 j += 1
@@ -313,7 +328,7 @@ def stage_breakdown(run, st, steps, peaks):
     """Per-stage times from a loop with an event at every stage boundary (a
     separate loop from the headline one, so its events do not perturb it)."""
     torch = run.torch
-    names = STAGES + (("backward",) if run.train else ())
+    names = run.names
     evs = _events(torch, steps, len(names) + 1)
     timed(torch, st, steps, lambda i: run.step(st, evs[i], marks=names + ("end",)))
     ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
@@ -344,6 +359,8 @@ def stages_cold_l2(run, st, peaks, reps=10):
     byt = stage_bytes(run.wl, R, with_probs=run.train)
     out = {}
     for n in ("gate", "dispatch", "combine"):
+        if n not in run.names:
+            continue
         t = []
         for i in range(reps):
             flush.fill_(i & 0xff)
@@ -423,9 +440,15 @@ def run_gpu(args):
     ms = max_over_ranks(ms)
     ffn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ffn_ev)
 
-    # ---- the same K steps through the single moe_forward call
+    # ---- the same K steps through the single moe_forward call, and through
+    # moe_forward with an x_disp buffer (the dispatch as its own copy kernel)
     fwd_call_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
         cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, run.bufs, run.ws, st)))
+    bufs_copy = L.alloc_buffers(cfg, dev)
+    bufs_copy["logits"] = None
+    copy_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
+        cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, bufs_copy, run.ws, st)))
+    del bufs_copy
     stages = stage_breakdown(run, st, args.steps, peaks)
     cold = stages_cold_l2(run, st, peaks)
     rstats = routing_stats(run)
@@ -464,6 +487,8 @@ def run_gpu(args):
     decode = decode_step(args, dev, max_over_ranks, world, peaks)
     residual = residual_step(args, dev, run, max_over_ranks, world)
     gpu_idx = run.bufs["topk_idx"].cpu().numpy()
+    run_fused = run.fused
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     del run
     torch.cuda.empty_cache()
     configs = {}
@@ -530,7 +555,9 @@ def run_gpu(args):
                 "timing": "CUDA events: before the first host-to-device copy, after the last "
                           "device-to-host copy"},
         "moe_forward_ms_per_step": fwd_call_ms / args.steps,
-        "gpu_launches": forward_launches(wl) * args.steps,
+        "moe_forward_with_dispatch_copy_ms_per_step": copy_ms / args.steps,
+        "dispatch": "fused into the first expert GEMM" if run_fused else "copy kernel",
+        "gpu_launches": forward_launches(wl, run_fused, num_sms) * args.steps,
         "clocks": clocks,
         "configs": configs,
         "decode_step": decode,
@@ -586,7 +613,7 @@ def residual_step(args, dev, run, max_over_ranks, world):
     wl, cfg, d = run.wl, run.cfg, run.d
     rw = [t.to(dev) for t in make_residual_weights(wl)]
     mix_w, mix_b = [t.to(dev) for t in make_residual_mix(wl)]
-    bufs = L.alloc_buffers(cfg, dev)
+    bufs = L.alloc_buffers(cfg, dev, fused_dispatch=wl.dtype == "bf16")
     bufs["logits"] = None
     ws = L.alloc_workspace(cfg, dev)
     y = torch.empty_like(d.x)

@@ -152,3 +152,28 @@ def test_residual_mix_argument_checks():
     assert call(None, None, FAKE) == N.MOE_ERR_INVALID_ARG
     assert call(MISALIGNED, FAKE, FAKE) == N.MOE_ERR_INVALID_ARG
     assert call(FAKE, FAKE, MISALIGNED) == N.MOE_ERR_INVALID_ARG
+
+
+def test_fused_dispatch_argument_checks():
+    """moe_expert_ffn_gather checks every pointer on the host and refuses fp32
+    layers (the gather form is a tensor-core GEMM); moe_forward without an
+    x_disp buffer is refused for an fp32 layer.  Nothing is enqueued."""
+    lib = N.library()
+    f32 = N.make_config(64, 32, 64, 4, 1, 1.0, 4, True, "relu", "f32")
+    bf = N.make_config(64, 32, 64, 4, 1, 1.0, 4, True, "relu", "bf16")
+
+    def gather(cfg, **o):
+        names = ("x", "row_src", "offsets", "w1", "b1", "w2", "b2")
+        return lib.moe_expert_ffn_gather(ctypes.byref(cfg), *[o.get(n, FAKE) for n in names],
+                                         o.get("h_pre"), o.get("h", FAKE), o.get("out", FAKE),
+                                         None)
+
+    assert gather(f32) == N.MOE_ERR_UNSUPPORTED
+    assert gather(bf, row_src=None) == N.MOE_ERR_INVALID_ARG
+    assert gather(bf, x=MISALIGNED) == N.MOE_ERR_INVALID_ARG
+    assert gather(bf, h_pre=MISALIGNED) == N.MOE_ERR_INVALID_ARG
+    assert gather(bf, out=None) == N.MOE_ERR_INVALID_ARG
+    nodisp = N.MoeBuffers(*([FAKE] * 14))
+    nodisp.x_disp = None
+    assert lib.moe_forward(ctypes.byref(f32), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                           ctypes.byref(nodisp), FAKE, 1 << 40, None) == N.MOE_ERR_INVALID_ARG

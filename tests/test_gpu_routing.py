@@ -140,3 +140,31 @@ def test_routing_scan_256_experts(base, S):
     assert np.allclose(f64(b["topk_w"]), g["weights"], rtol=2e-6, atol=1e-7)
     assert abs(float(b["l_aux"].item()) - g["l_aux"]) <= 1e-5 * abs(g["l_aux"])
     assert N.moe_get_device_error() == 0
+
+
+def test_gate_on_two_streams_at_once():
+    """Two single-launch gates in flight on different streams (each takes its
+    own grid-barrier words) give the same routing as the same calls made one
+    after the other; repeated calls reuse the barrier words cleanly."""
+    wls = [WORKLOADS["e64_bf16"].scaled(9000), WORKLOADS["skew_e16_drop"].scaled(7000)]
+    runs = [GpuRun(w) for w in wls]      # serial reference calls
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for w, r in zip(wls, runs):
+        b = L.alloc_buffers(r.cfg, DEV)
+        outs.append((b, L.alloc_workspace(r.cfg, DEV)))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (b, ws), r, st in zip(outs, runs, streams):
+            d = r.d
+            N.moe_gate_topk(r.cfg, d.x, d.w_gate, d.logit_bias, b["logits"], None, b["topk_idx"],
+                            b["topk_w"], b["slot"], b["routed_cnt"], b["kept_cnt"],
+                            b["expert_offsets"], b["row_src"], b["l_aux"], ws, st)
+    torch.cuda.synchronize()
+    for (b, _), r in zip(outs, runs):
+        for key in ("topk_idx", "slot", "routed_cnt", "kept_cnt", "expert_offsets", "topk_w",
+                    "l_aux"):
+            assert torch.equal(b[key], r.bufs[key]), key
+        R = r.num_rows
+        assert torch.equal(b["row_src"][:R], r.bufs["row_src"][:R])
+    assert N.moe_get_device_error() == 0
