@@ -123,15 +123,17 @@ class ClockSampler:
         self.handle = None
         self.nvml = None
         self.source = "none"
+        self.nvml_error = None
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nvml = pynvml
             self.handle = self._handle(pynvml)
             self.sm_max = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
+            self.nvml = pynvml
             self.source = "nvml"
-        except Exception:
+        except Exception as e:  # noqa: BLE001  (reported in the clocks record)
             self.nvml = None
+            self.nvml_error = f"{type(e).__name__}: {e}"
 
     def _handle(self, pynvml):
         try:
@@ -182,6 +184,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "source": self.source}
 
     def _smi_once(self):
+        rec = self._smi_query()
+        if self.nvml_error:
+            rec["nvml_error"] = self.nvml_error
+        return rec
+
+    def _smi_query(self):
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
@@ -351,10 +359,13 @@ def stage_breakdown(run, st, steps, peaks):
 
 def stages_cold_l2(run, st, peaks, reps=10):
     """Gate, dispatch and combine launched alone with L2 flushed before each
-    launch (a 512 MB write): their HBM bandwidth without help from data
-    that an earlier stage left in the 126 MB L2."""
+    launch: their HBM bandwidth without help from data that an earlier stage
+    left in the 126 MB L2.  The flush READS a 512 MB buffer, so the L2 holds
+    clean lines and no write-back of the flush lands inside the timed
+    launch."""
     torch = run.torch
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=run.d.x.device)
+    flush = torch.ones(512 << 20, dtype=torch.uint8, device=run.d.x.device)
+    flush.max()
     R = run.rows()
     byt = stage_bytes(run.wl, R, with_probs=run.train)
     out = {}
@@ -363,7 +374,7 @@ def stages_cold_l2(run, st, peaks, reps=10):
             continue
         t = []
         for i in range(reps):
-            flush.fill_(i & 0xff)
+            flush.max()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
             run.stage(n, st)

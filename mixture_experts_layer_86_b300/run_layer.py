@@ -2,10 +2,12 @@
 the C ABI -- a fixed, small command for profilers and quick checks.
 
     python -m mixture_experts_layer_86_b300.run_layer --workload e64_bf16 \\
-        [--tokens S] [--experts E] [--iters N] [--backward] [--stage gate]
+        [--tokens S] [--experts E] [--iters N] [--backward] [--fused] [--stage gate]
 
 --tokens / --experts shrink the batch / the number of experts of a named
 workload while keeping the per-expert shape (d, f, k, capacity factor).
+--fused runs the forward without the x_disp copy (the dispatch fused into the
+first expert GEMM; bf16 forward only).
 --stage gate runs only moe_gate_topk and allocates only what it needs (x,
 W_g, the routing outputs and the workspace), so a profiler that saves and
 restores device memory between its passes has little to move.
@@ -52,6 +54,7 @@ def main():
     ap.add_argument("--experts", type=int, default=None)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--backward", action="store_true")
+    ap.add_argument("--fused", action="store_true")
     ap.add_argument("--stage", default="forward", choices=["forward", "gate"])
     a = ap.parse_args()
     wl = WORKLOADS[a.workload]
@@ -64,7 +67,8 @@ def main():
     else:
         inp = make_inputs(wl, with_dy=a.backward).to("cuda:0")
         cfg = N.config_from_workload(wl)
-        bufs = L.alloc_buffers(cfg, "cuda:0", training=a.backward)
+        bufs = L.alloc_buffers(cfg, "cuda:0", training=a.backward,
+                               fused_dispatch=a.fused and not a.backward)
         ws = L.alloc_workspace(cfg, "cuda:0", for_backward=False)
         wsb = L.alloc_workspace(cfg, "cuda:0", for_backward=True) if a.backward else None
         for _ in range(a.iters):
