@@ -54,6 +54,26 @@ R10 The gate temperature T (gating_softmax_temp) divides the logits before
     the softmax; the top-k choice (taken on the logits) is unchanged.
     Noisy gating adds caller-drawn noise to the logits as a per-token bias
     [S,E] (the layer itself stays deterministic; the noise gets no gradient).
+R11 In-layer randomness (``noisy_gate_policy``, ``use_rts``,
+    ``top2_2nd_expert_sampling``, named on the deepspeed.moe overview §2.1
+    without formulas) comes from Philox4x32-10 keyed by a seed and an offset
+    (``random_streams``).  noisy_gate_policy = "rsample": the experts are
+    chosen as the top-k of logits + g, g[s,e] standard Gumbel noise (the
+    Gumbel-max sample of the softmax); the keys are formed in float32, the
+    precision of the logits; probabilities and combine weights stay those of
+    the noise-free logits.  The noise is a constant of the backward.
+R12 noisy_gate_policy = "jitter": the router sees x~ = x * f, f[s,c] =
+    1 + eps * (2u - 1) (eps = 0.01 unless configured), computed in float32
+    and, for a bf16 layer, rounded to bf16; the experts see x.  Backward:
+    dW_g = dlogits^T x~ and the router's part of dX is (dlogits W_g) * f.
+R13 top2_2nd_expert_sampling: the first choice is the noise-free arg-max;
+    the second is the arg-max of the float32 keys logits + g over the other
+    experts.
+R14 use_rts (random token selection): the capacity queue takes every first
+    choice before every second choice, as in R4, but within a choice level
+    the tokens come in the order of a keyed pseudorandom permutation pi
+    (a Feistel network over Philox, cycle-walked to [0, S)) instead of token
+    order; rows of the expert-major buffer follow the queue.
 
 Parity pins (tests/test_oracle_pins.py): brute-force top-k and slot
 enumeration on tiny inputs, hand-worked capacity/drop cases, the pages' own
@@ -69,6 +89,8 @@ from fractions import Fraction
 from typing import Optional
 
 import numpy as np
+
+from . import random_streams as RS
 
 ACT_RELU = "relu"
 ACT_GELU_TANH = "gelu_tanh"
@@ -198,7 +220,7 @@ class Routing:
 
 
 def assign_slots(idx: np.ndarray, num_experts: int,
-                 cap: Optional[int]) -> Routing:
+                 cap: Optional[int], order=None) -> Routing:
     """Capacity-limited slot assignment in priority order (reading R4).
 
     One counter per expert; walk choice j = 0..k-1 (outer) and token
@@ -206,12 +228,15 @@ def assign_slots(idx: np.ndarray, num_experts: int,
     counter advances whether or not the slot is kept.  Kept iff slot < C
     ([deepspeed.moe overview] §2.1 drop_tokens; [MoE explainer] §3.1 "Drop
     tokens").  Rows of the expert-major buffer are offsets[e] + slot.
+    ``order``: the tokens in queue order within a choice level (random token
+    selection, reading R14); token order when None.
     """
     S, k = idx.shape
     counter = [0] * num_experts
     slot = np.full((S, k), -1, np.int64)
+    tokens = range(S) if order is None else [int(t) for t in order]
     for j in range(k):
-        for s in range(S):
+        for s in tokens:
             e = int(idx[s, j])
             pos = counter[e]
             counter[e] += 1
@@ -331,17 +356,73 @@ class LayerConfig:
     aux_loss_weight: float = 0.0
     gate_temperature: float = 1.0   # p = softmax(logits / T) (reading R10)
     aux_loss_type: str = "load"     # "load" | "std"
+    noise_policy: str = "none"      # "none" | "jitter" | "rsample" (R11, R12)
+    second_expert_sampling: bool = False   # R13
+    use_rts: bool = False           # R14
+    noise_seed: int = 0
+    noise_offset: int = 0
+    jitter_eps: float = 0.01
+    dtype: str = "bf16"             # the router input's storage under jitter: bf16 | f32 | f64
 
 
-def route(logits: np.ndarray, cfg: LayerConfig) -> dict:
+def selection_noise(cfg: LayerConfig, num_tokens: int) -> Optional[np.ndarray]:
+    """The Gumbel noise g[s,e] the choice uses (R11, R13), or None."""
+    if cfg.noise_policy == "rsample" or (cfg.second_expert_sampling and cfg.k == 2):
+        return RS.gate_noise(num_tokens, cfg.num_experts, cfg.noise_seed, cfg.noise_offset)[1]
+    return None
+
+
+def select_experts(logits: np.ndarray, cfg: LayerConfig, noise=None) -> np.ndarray:
+    """The k chosen experts per token under the gate-noise options: plain
+    top-k of the logits; top-k of the float32 keys logits + g (rsample,
+    R11); or the noise-free first choice and the second from the keys
+    (second-expert sampling, R13).  ``noise``: g (float, [S,E]); drawn from
+    the layer's stream when None."""
+    lg = np.asarray(logits, np.float64)
+    S = lg.shape[0]
+    if noise is None:
+        noise = selection_noise(cfg, S)
+    if noise is None:
+        return topk_experts(lg, cfg.k)
+    keys = (lg.astype(np.float32) + np.asarray(noise).astype(np.float32)).astype(np.float64)
+    if cfg.noise_policy == "rsample":
+        return topk_experts(keys, cfg.k)
+    first = topk_experts(lg, 1)[:, 0]
+    rest = keys.copy()
+    rest[np.arange(S), first] = -np.inf
+    second = np.argmax(rest, axis=1)        # ties to the lower index
+    return np.stack([first, second], axis=1)
+
+
+def router_input(x: np.ndarray, cfg: LayerConfig):
+    """(x~, f): the router's input and the jitter factors (R12); (x, None)
+    without jitter."""
+    x = np.asarray(x, np.float64)
+    if cfg.noise_policy != "jitter":
+        return x, None
+    S, d = x.shape
+    f = RS.jitter_factors(S, d, cfg.jitter_eps, cfg.noise_seed, cfg.noise_offset)
+    if cfg.dtype == "f64":
+        return x * f.astype(np.float64), f
+    prod = x.astype(np.float32) * f                     # one float32 rounding
+    if cfg.dtype == "bf16":
+        import torch
+        prod = torch.from_numpy(prod).to(torch.bfloat16).to(torch.float32).numpy()
+    return prod.astype(np.float64), f
+
+
+def route(logits: np.ndarray, cfg: LayerConfig, noise=None) -> dict:
     """Gate stages after the logits: softmax, top-k, weights, slots, l_aux."""
     S, E = logits.shape
     probs = softmax(np.asarray(logits, np.float64) / cfg.gate_temperature)
-    idx = topk_experts(logits, cfg.k)
+    idx = select_experts(logits, cfg, noise)
     w = gate_weights(probs, idx)
     cap = capacity(S, E, cfg.k, cfg.capacity_factor, cfg.min_capacity,
                    cfg.drop_tokens)
-    rt = assign_slots(idx, E, cap)
+    order = None
+    if cfg.use_rts:
+        order = np.argsort(RS.rts_position(S, cfg.noise_seed, cfg.noise_offset), kind="stable")
+    rt = assign_slots(idx, E, cap, order)
     return {"logits": np.asarray(logits, np.float64), "probs": probs,
             "weights": w, "routing": rt, "l_aux": aux_loss(probs, idx, cfg.aux_loss_type)}
 
@@ -357,7 +438,7 @@ def forward(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, logit_bias=None,
     """
     x = np.asarray(x, np.float64)
     if logits is None:
-        logits = gate_logits(x, w_gate, logit_bias)
+        logits = gate_logits(router_input(x, cfg)[0], w_gate, logit_bias)
     g = route(logits, cfg)
     rt = g["routing"]
     x_disp = dispatch(x, rt)
@@ -374,9 +455,9 @@ def dense_mixture(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, logit_bias=None):
     §6.5 compare MoE against a dense computation).  Equals ``forward`` when
     ``drop_tokens`` is false."""
     x = np.asarray(x, np.float64)
-    lg = gate_logits(x, w_gate, logit_bias)
+    lg = gate_logits(router_input(x, cfg)[0], w_gate, logit_bias)
     p = softmax(lg / cfg.gate_temperature)
-    idx = topk_experts(lg, cfg.k)
+    idx = select_experts(lg, cfg)
     w = gate_weights(p, idx)
     S, E = lg.shape
     mix = np.zeros((S, E), np.float64)
@@ -515,8 +596,12 @@ def backward(cfg: LayerConfig, fwd: dict, x, w_gate, w1, w2, dy) -> dict:
 
     # p = softmax(logits / T): the logits' gradient carries the 1/T
     dlogits = p * (dp - np.sum(dp * p, axis=1, keepdims=True)) / cfg.gate_temperature
-    dw_gate = dlogits.T @ x
+    # the router saw x~ = x * f under jitter (R12)
+    xr, jf = router_input(x, cfg)
+    dw_gate = dlogits.T @ xr
     dx = dlogits @ w_gate
+    if jf is not None:
+        dx = dx * jf.astype(np.float64)
     for s in range(S):
         for j in range(k):
             r = rt.row_of(s, j)
@@ -534,7 +619,7 @@ def loss(cfg: LayerConfig, x, w_gate, w1, b1, w2, b2, dy, logit_bias=None,
     counts) to that of a previous forward, so that a perturbation cannot move
     a token between experts."""
     x = np.asarray(x, np.float64)
-    lg = gate_logits(x, w_gate, logit_bias)
+    lg = gate_logits(router_input(x, cfg)[0], w_gate, logit_bias)
     p = softmax(lg / cfg.gate_temperature)
     if routing_from is None:
         g = route(lg, cfg)
