@@ -70,6 +70,12 @@ typedef enum {
   MOE_AUX_STD = 1   /* l_aux = std_e(mean_s p[s,e]) + 1e-6 (population std)    */
 } moe_aux_loss;
 
+typedef enum {
+  MOE_NOISE_NONE = 0,
+  MOE_NOISE_JITTER = 1,  /* router input x * U(1-eps, 1+eps)                   */
+  MOE_NOISE_RSAMPLE = 2  /* choose the top-k of logits + Gumbel noise          */
+} moe_noise_policy;
+
 /* Mirrors MoE(hidden_size, num_experts, k, capacity_factor, min_capacity,
  * drop_tokens) of the deepspeed.moe overview, §2.1, plus the expert FFN
  * width, activation, element type and the weight of l_aux in the training
@@ -80,11 +86,28 @@ typedef enum {
  *  - aux_loss_type: the balance loss of the layer's specification, or the
  *    DeepSeek-MoE page's std-based alternative lambda * (std(usage) + 1e-6)
  *    with usage[e] = mean over tokens of p[s,e] (ch.1 load-balancing table).
- *  - logit_bias_per_token: logit_bias is [S,E] instead of [E].  Noisy gating
- *    (noisy_gate_policy, deepspeed.moe overview §2.1 / §3.1) adds random
- *    noise to the gate logits; the caller draws that noise and passes it
- *    here, so the layer itself stays deterministic.  A per-token bias gets
- *    no gradient. */
+ *  - logit_bias_per_token: logit_bias is [S,E] instead of [E]: noise the
+ *    caller draws itself and adds to the gate logits.  A per-token bias gets
+ *    no gradient.
+ * and the randomised gate options the overview names in §2.1 without
+ * formulas, drawn inside the layer from Philox4x32-10 (Salmon et al., SC
+ * 2011) keyed by noise_seed and noise_offset, so a run is reproducible:
+ *  - noise_policy (noisy_gate_policy): MOE_NOISE_RSAMPLE chooses the experts
+ *    as the top-k of the float32 keys logits + g, g standard Gumbel noise
+ *    (a sample of the softmax); probabilities and combine weights stay those
+ *    of the noise-free logits.  MOE_NOISE_JITTER feeds the router x * f,
+ *    f = 1 + jitter_eps * (2u - 1) per element (float32, then rounded to the
+ *    layer type); the experts see x.
+ *  - second_expert_sampling (top2_2nd_expert_sampling, k = 2): the first
+ *    choice stays the arg-max logit, the second is the arg-max of logits + g
+ *    over the other experts.
+ *  - use_rts (random token selection): each expert's capacity queue takes
+ *    the first choices, then the second choices, each in a keyed random
+ *    order of the tokens (a Philox Feistel permutation) instead of token
+ *    order, so which tokens are dropped is random.
+ * The noise is a constant of the backward (jitter: dW_g uses x * f and the
+ * router's part of dX is multiplied by f).  moe_gate_noise returns the draws
+ * of a configuration. */
 typedef struct {
   int64_t num_tokens;      /* S >= 0                                        */
   int32_t hidden_size;     /* d                                             */
@@ -100,6 +123,12 @@ typedef struct {
   float gate_temperature;  /* >= 0; 0 or 1 = plain softmax                   */
   int32_t aux_loss_type;   /* moe_aux_loss                                   */
   int32_t logit_bias_per_token; /* nonzero: logit_bias is [S,E], else [E]    */
+  int32_t noise_policy;    /* moe_noise_policy                               */
+  int32_t second_expert_sampling; /* nonzero (k = 2 only): sampled 2nd choice */
+  int32_t use_rts;         /* nonzero: random token selection                */
+  float jitter_eps;        /* MOE_NOISE_JITTER half-width; 0 means 0.01      */
+  uint64_t noise_seed;     /* Philox key                                     */
+  uint64_t noise_offset;   /* Philox counter words 2-3 (a new draw per step) */
 } moe_config;
 
 /* Saved state of one forward pass (all device pointers, caller-owned).
@@ -193,6 +222,16 @@ moe_status moe_gate_topk_static(const moe_config *cfg, const void *x,
                                 int32_t *kept_cnt, int32_t *expert_offsets,
                                 int32_t *row_src, float *l_aux,
                                 moe_stream_t stream);
+
+/* The random draws the gate makes for this configuration (no other
+ * output): uniform [S,E] fp32, the uniforms u of the gate-noise stream;
+ * gumbel [S,E] fp32, -ln(-ln u) as the gate adds them to the logits under
+ * MOE_NOISE_RSAMPLE or second-expert sampling; position [S] int32, the
+ * queue position of each token under random token selection.  Each may be
+ * NULL.  The values do not depend on the noise options that are set; the
+ * gate uses them only where its options say so. */
+moe_status moe_gate_noise(const moe_config *cfg, float *uniform, float *gumbel,
+                          int32_t *position, moe_stream_t stream);
 
 /* The routing half of moe_gate_topk, taking the logits as input instead of
  * computing them (the same kernels; used to check routing bit for bit

@@ -20,6 +20,8 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_RELU, MOE_ACT_GELU_TANH, MOE_ACT_GELU_ERF = 0, 1, 2
 MOE_AUX_LOAD, MOE_AUX_STD = 0, 1
 AUX_CODES = {"load": MOE_AUX_LOAD, "std": MOE_AUX_STD}
+MOE_NOISE_NONE, MOE_NOISE_JITTER, MOE_NOISE_RSAMPLE = 0, 1, 2
+NOISE_CODES = {"none": MOE_NOISE_NONE, "jitter": MOE_NOISE_JITTER, "rsample": MOE_NOISE_RSAMPLE}
 ACT_CODES = {"relu": MOE_ACT_RELU, "gelu_tanh": MOE_ACT_GELU_TANH, "gelu_erf": MOE_ACT_GELU_ERF}
 DTYPE_CODES = {"f32": MOE_F32, "bf16": MOE_BF16}
 
@@ -29,7 +31,10 @@ class MoeConfig(ctypes.Structure):
                 ("num_experts", c_int32), ("k", c_int32), ("capacity_factor", c_double),
                 ("min_capacity", c_int32), ("drop_tokens", c_int32), ("act", c_int32),
                 ("dtype", c_int32), ("aux_loss_weight", c_float), ("gate_temperature", c_float),
-                ("aux_loss_type", c_int32), ("logit_bias_per_token", c_int32)]
+                ("aux_loss_type", c_int32), ("logit_bias_per_token", c_int32),
+                ("noise_policy", c_int32), ("second_expert_sampling", c_int32),
+                ("use_rts", c_int32), ("jitter_eps", c_float), ("noise_seed", ctypes.c_uint64),
+                ("noise_offset", ctypes.c_uint64)]
 
 
 class MoeBuffers(ctypes.Structure):
@@ -57,6 +62,7 @@ _SIGS = {
     "moe_workspace_size": (c_int, [POINTER(MoeConfig), c_int, POINTER(c_size_t)]),
     "moe_gate_topk": (c_int, [POINTER(MoeConfig)] + [_P] * 14 + [c_size_t, _P]),
     "moe_route_from_logits": (c_int, [POINTER(MoeConfig)] + [_P] * 11 + [c_size_t, _P]),
+    "moe_gate_noise": (c_int, [POINTER(MoeConfig)] + [_P] * 3 + [_P]),
     "moe_gate_topk_static": (c_int, [POINTER(MoeConfig)] + [_P] * 13 + [_P]),
     "moe_dispatch": (c_int, [POINTER(MoeConfig)] + [_P] * 5 + [_P]),
     "moe_expert_ffn": (c_int, [POINTER(MoeConfig)] + [_P] * 9 + [_P]),
@@ -114,14 +120,20 @@ def _stream(stream):
 def make_config(num_tokens, hidden_size, ffn_size, num_experts, k, capacity_factor,
                 min_capacity, drop_tokens, act="gelu_tanh", dtype="bf16",
                 aux_loss_weight=0.0, gate_temperature=1.0, aux_loss_type="load",
-                logit_bias_per_token=False) -> MoeConfig:
+                logit_bias_per_token=False, noise_policy="none",
+                second_expert_sampling=False, use_rts=False, jitter_eps=0.01,
+                noise_seed=0, noise_offset=0) -> MoeConfig:
     return MoeConfig(int(num_tokens), int(hidden_size), int(ffn_size), int(num_experts), int(k),
                      float(capacity_factor), int(min_capacity), int(bool(drop_tokens)),
                      ACT_CODES[act] if isinstance(act, str) else int(act),
                      DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype),
                      float(aux_loss_weight), float(gate_temperature),
                      AUX_CODES[aux_loss_type] if isinstance(aux_loss_type, str)
-                     else int(aux_loss_type), int(bool(logit_bias_per_token)))
+                     else int(aux_loss_type), int(bool(logit_bias_per_token)),
+                     NOISE_CODES[noise_policy] if isinstance(noise_policy, str)
+                     else int(noise_policy), int(bool(second_expert_sampling)),
+                     int(bool(use_rts)), float(jitter_eps), int(noise_seed) & (2 ** 64 - 1),
+                     int(noise_offset) & (2 ** 64 - 1))
 
 
 def config_from_workload(wl, num_tokens=None) -> MoeConfig:
@@ -129,7 +141,11 @@ def config_from_workload(wl, num_tokens=None) -> MoeConfig:
                        wl.ffn_size, wl.num_experts, wl.k, wl.capacity_factor, wl.min_capacity,
                        wl.drop_tokens, wl.act, wl.dtype, wl.aux_loss_weight,
                        getattr(wl, "gate_temperature", 1.0), getattr(wl, "aux_loss_type", "load"),
-                       getattr(wl, "logit_noise_std", 0.0) > 0)
+                       getattr(wl, "logit_noise_std", 0.0) > 0,
+                       getattr(wl, "noise_policy", "none"),
+                       getattr(wl, "second_expert_sampling", False),
+                       getattr(wl, "use_rts", False), getattr(wl, "jitter_eps", 0.01),
+                       getattr(wl, "noise_seed", 0), getattr(wl, "noise_offset", 0))
 
 
 # ---------------------------------------------------------------- host-only
@@ -170,6 +186,13 @@ def moe_gate_topk_static(cfg, x, w_gate, logit_bias, logits, probs, topk_idx, to
         ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(logit_bias), _ptr(logits), _ptr(probs),
         _ptr(topk_idx), _ptr(topk_w), _ptr(slot), _ptr(routed_cnt), _ptr(kept_cnt),
         _ptr(expert_offsets), _ptr(row_src), _ptr(l_aux), _stream(stream)))
+
+
+def moe_gate_noise(cfg, uniform=None, gumbel=None, position=None, stream=None):
+    """The gate's random draws for cfg: uniforms and Gumbel noise [S,E] fp32,
+    random-token-selection queue positions [S] int32 (each optional)."""
+    _check("moe_gate_noise", _lib.moe_gate_noise(
+        ctypes.byref(cfg), _ptr(uniform), _ptr(gumbel), _ptr(position), _stream(stream)))
 
 
 def moe_route_from_logits(cfg, logits, probs, topk_idx, topk_w, slot, routed_cnt, kept_cnt,

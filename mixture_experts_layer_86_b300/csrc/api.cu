@@ -19,6 +19,24 @@ float inv_temperature(const moe_config *c) {
   return c->gate_temperature > 0.0f ? 1.0f / c->gate_temperature : 1.0f;
 }
 
+RouteNoise noise_of(const moe_config *c) {
+  RouteNoise n{};
+  n.policy = c->noise_policy;
+  n.second = c->k == 2 ? c->second_expert_sampling : 0;
+  n.rts = c->use_rts;
+  n.jitter_eps = c->jitter_eps;
+  n.seed = c->noise_seed;
+  n.offset = c->noise_offset;
+  return n;
+}
+
+// bytes of the jittered router input (only under MOE_NOISE_JITTER)
+size_t jitter_bytes(const moe_config *c) {
+  return c->noise_policy == MOE_NOISE_JITTER
+             ? align256(size_t(c->num_tokens) * c->hidden_size * elem_bytes(c->dtype))
+             : 0;
+}
+
 unsigned int *device_error_ptr() {
   static PerDevice<unsigned int *> ptrs;
   unsigned int *p = nullptr;
@@ -49,6 +67,12 @@ moe_status check_config(const moe_config *c) {
   if (c->aux_loss_type != MOE_AUX_LOAD && c->aux_loss_type != MOE_AUX_STD)
     return MOE_ERR_INVALID_ARG;
   if (c->logit_bias_per_token != 0 && c->logit_bias_per_token != 1) return MOE_ERR_INVALID_ARG;
+  if (c->noise_policy < MOE_NOISE_NONE || c->noise_policy > MOE_NOISE_RSAMPLE)
+    return MOE_ERR_INVALID_ARG;
+  if ((c->second_expert_sampling != 0 && c->second_expert_sampling != 1) ||
+      (c->use_rts != 0 && c->use_rts != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (!(c->jitter_eps >= 0.0f && c->jitter_eps < 1.0f)) return MOE_ERR_INVALID_ARG;
   if (c->num_experts > kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (c->num_tokens * c->k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -72,28 +96,39 @@ int64_t max_rows_of(const moe_config *c) {
   return ec < sk ? ec : sk;
 }
 
+// forward workspace: routing scratch | logits scratch | jittered input
 size_t fwd_ws_bytes(const moe_config *c) {
   return route_workspace_bytes(c->num_tokens, c->num_experts, c->k) +
-         align256(size_t(c->num_tokens) * c->num_experts * 4);  // logits scratch
+         align256(size_t(c->num_tokens) * c->num_experts * 4) + jitter_bytes(c);
+}
+float *fwd_ws_logits(const moe_config *c, void *ws) {
+  return reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                   route_workspace_bytes(c->num_tokens, c->num_experts, c->k));
+}
+void *fwd_ws_jitter(const moe_config *c, void *ws) {
+  return static_cast<char *>(ws) + route_workspace_bytes(c->num_tokens, c->num_experts, c->k) +
+         align256(size_t(c->num_tokens) * c->num_experts * 4);
 }
 
 struct BwdWs {
   void *d_out, *dh_pre, *dx_disp;
   float *dw, *dlogits, *gate_partial;
   float *aux_coef;
+  void *xj;  // the jittered router input (MOE_NOISE_JITTER only)
 };
 
 size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const int64_t R = max_rows_of(c);
   const size_t eb = elem_bytes(c->dtype);
-  const size_t sz[7] = {align256(size_t(R) * c->hidden_size * eb),
+  const size_t sz[8] = {align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(c->num_tokens) * c->k * 4),
                         align256(size_t(c->num_tokens) * c->num_experts * 4),
                         align256(gate_wgrad_partial_bytes(c->num_tokens, c->num_experts,
                                                           c->hidden_size)),
-                        align256(size_t(c->num_experts) * 4)};
+                        align256(size_t(c->num_experts) * 4),
+                        jitter_bytes(c)};
   if (w) {
     char *p = static_cast<char *>(base);
     w->d_out = p; p += sz[0];
@@ -102,7 +137,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->dw = reinterpret_cast<float *>(p); p += sz[3];
     w->dlogits = reinterpret_cast<float *>(p); p += sz[4];
     w->gate_partial = reinterpret_cast<float *>(p); p += sz[5];
-    w->aux_coef = reinterpret_cast<float *>(p);
+    w->aux_coef = reinterpret_cast<float *>(p); p += sz[6];
+    w->xj = sz[7] ? p : nullptr;
   }
   size_t total = 0;
   for (size_t v : sz) total += v;
@@ -145,6 +181,7 @@ moe_status route(const moe_config *c, const float *logits, float *probs, int32_t
   a.aux_type = c->aux_loss_type;
   a.probs = probs; a.idx = idx; a.w = w; a.slot = slot;
   a.routed = routed; a.kept = kept; a.offsets = offsets; a.row_src = row_src; a.l_aux = l_aux;
+  a.noise = noise_of(c);
   route_carve_workspace(a, ws);
   return cuda_status(launch_route(a, st));
 }
@@ -310,6 +347,14 @@ moe_status moe_workspace_size(const moe_config *cfg, int for_backward, size_t *b
   return MOE_OK;
 }
 
+moe_status moe_gate_noise(const moe_config *cfg, float *uniform, float *gumbel,
+                          int32_t *position, moe_stream_t stream) {
+  MOE_TRY(check_config(cfg));
+  if (!ok_opt(uniform) || !ok_opt(gumbel) || !ok_opt(position)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_gate_noise(cfg->num_tokens, cfg->num_experts, noise_of(cfg), uniform,
+                                       gumbel, position, stream));
+}
+
 moe_status moe_route_from_logits(const moe_config *cfg, const float *logits, float *probs,
                                  int32_t *topk_idx, float *topk_w, int32_t *slot,
                                  int32_t *routed_cnt, int32_t *kept_cnt, int32_t *expert_offsets,
@@ -337,6 +382,39 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x, const void *w_gat
       !ok_ptr(l_aux) || !ok_ptr(workspace))
     return MOE_ERR_INVALID_ARG;
   if (workspace_bytes < fwd_ws_bytes(cfg)) return MOE_ERR_WORKSPACE;
+  const RouteNoise noise = noise_of(cfg);
+  if (noise.any()) {
+    // randomised gate: (jitter the router input,) the router GEMM writes
+    // the logits, then the routing kernels draw the noise / take the
+    // random queue order
+    const void *xr = x;
+    if (noise.policy == MOE_NOISE_JITTER) {
+      void *xj = fwd_ws_jitter(cfg, workspace);
+      MOE_CUDA(launch_jitter(x, cfg->dtype, cfg->num_tokens, cfg->hidden_size, noise, xj,
+                             stream));
+      xr = xj;
+    }
+    float *lg = logits ? logits : fwd_ws_logits(cfg, workspace);
+    if (cfg->dtype == MOE_BF16) {
+      // the tensor-core gate kernel for the logits; its routing outputs are
+      // rewritten by the routing kernels below
+      RouteArgs a{};
+      a.S = cfg->num_tokens; a.E = cfg->num_experts; a.k = cfg->k;
+      route_carve_workspace(a, workspace);
+      GateTcArgs g{};
+      g.x = xr; g.w_gate = w_gate; g.S = cfg->num_tokens; g.d = cfg->hidden_size;
+      g.E = cfg->num_experts; g.k = cfg->k; g.logit_bias = logit_bias; g.logits = lg;
+      g.bias_ld = cfg->logit_bias_per_token ? cfg->num_experts : 0;
+      g.inv_temp = inv_temperature(cfg);
+      g.probs = nullptr; g.idx = topk_idx; g.w = topk_w; g.rank = slot; g.hist = a.hist;
+      g.psum = a.psum; g.err = device_error_ptr();
+      MOE_CUDA(launch_gate_tc(g, stream));
+    } else {
+      MOE_TRY(gate_gemm(cfg, xr, w_gate, logit_bias, lg, stream));
+    }
+    return route(cfg, lg, probs, topk_idx, topk_w, slot, routed_cnt, kept_cnt, expert_offsets,
+                 row_src, l_aux, workspace, stream);
+  }
   if (cfg->dtype == MOE_BF16) {
     // one launch: tensor-core gate, routing and slot assignment
     GateRouteArgs ga{};
@@ -368,10 +446,7 @@ moe_status moe_gate_topk(const moe_config *cfg, const void *x, const void *w_gat
     MOE_CUDA(launch_gate_tc(g, stream));
     return cuda_status(launch_route_finish(a, stream));
   }
-  float *lg = logits;
-  if (!lg)
-    lg = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                   route_workspace_bytes(cfg->num_tokens, cfg->num_experts, cfg->k));
+  float *lg = logits ? logits : fwd_ws_logits(cfg, workspace);
   MOE_TRY(gate_gemm(cfg, x, w_gate, logit_bias, lg, stream));
   return route(cfg, lg, probs, topk_idx, topk_w, slot, routed_cnt, kept_cnt, expert_offsets,
                row_src, l_aux, workspace, stream);
@@ -582,15 +657,22 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
       MOE_CUDA(launch_simt_gemm(g, st));
     }
   }
-  // 6. router: dlogits, dW_g = dlogits^T x
+  // 6. router: dlogits, dW_g = dlogits^T x (the router saw x * f under jitter)
   MOE_CUDA(launch_aux_coef(sv->topk_idx, sv->probs, S, k, E, cfg->aux_loss_type, w.aux_coef,
                            st));
   MOE_CUDA(launch_gate_bwd(sv->probs, sv->topk_idx, w.dw, w.aux_coef, S, E, k,
                            cfg->aux_loss_weight, inv_temperature(cfg), w.dlogits, st));
-  MOE_CUDA(launch_gate_wgrad(w.dlogits, x, dt, S, d, E, w.gate_partial, dw_gate, st));
-  // 7. dX = sum_j dx_disp[row] + dlogits W_g
+  const RouteNoise noise = noise_of(cfg);
+  const void *xr = x;
+  if (noise.policy == MOE_NOISE_JITTER) {
+    MOE_CUDA(launch_jitter(x, dt, S, d, noise, w.xj, st));
+    xr = w.xj;
+  }
+  MOE_CUDA(launch_gate_wgrad(w.dlogits, xr, dt, S, d, E, w.gate_partial, dw_gate, st));
+  // 7. dX = sum_j dx_disp[row] + (dlogits W_g) (* f under jitter)
   return cuda_status(launch_dx_combine(w.dx_disp, w.dlogits, w_gate, dt, S, d, E, k,
-                                       sv->topk_idx, sv->slot, sv->expert_offsets, dx, st));
+                                       sv->topk_idx, sv->slot, sv->expert_offsets, dx, st,
+                                       noise.policy == MOE_NOISE_JITTER ? &noise : nullptr));
 }
 
 moe_status moe_get_device_error(uint32_t *code) {

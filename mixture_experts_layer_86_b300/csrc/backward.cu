@@ -10,6 +10,7 @@
 // added in a fixed order, so the result is the same on every run.
 #include "common.cuh"
 #include "kernels.h"
+#include "rng.cuh"
 
 namespace moe {
 namespace {
@@ -106,7 +107,8 @@ __global__ void __launch_bounds__(kDxThreads)
 dx_combine_tile_kernel(const T *__restrict__ dx_disp, const float *__restrict__ dlogits,
                        const T *__restrict__ w_gate, int64_t S, int d, int E, int k,
                        const int32_t *__restrict__ idx, const int32_t *__restrict__ slot,
-                       const int32_t *__restrict__ offsets, T *__restrict__ dx) {
+                       const int32_t *__restrict__ offsets, T *__restrict__ dx, int jitter,
+                       RouteNoise noise) {
   griddep_begin();
   __shared__ __align__(16) float s_dlT[kDxE][kDxT];
   __shared__ __align__(16) float s_w[kDxE][kDxC];
@@ -170,6 +172,14 @@ dx_combine_tile_kernel(const T *__restrict__ dx_disp, const float *__restrict__ 
     const int t = ty * 8 + i;
     if (t >= nt) break;
     float v[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
+    if (jitter) {
+      // the router's input was x * f: its gradient is the router term * f
+      const uint4 w4 = rng::block(rng::make_key(noise.seed, noise.offset), rng::kPurposeJitter,
+                                  uint32_t(t0 + t), uint32_t(c >> 2));
+      const float eps = noise.jitter_eps > 0.0f ? noise.jitter_eps : 0.01f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] *= rng::jitter(rng::uniform(rng::word(w4, q)), eps);
+    }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int64_t r = s_row[t][j];
@@ -217,17 +227,19 @@ cudaError_t launch_gate_wgrad(const float *dlogits, const void *x, int dtype, in
 cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits, const void *w_gate,
                               int dtype, int64_t S, int d, int E, int k, const int32_t *idx,
                               const int32_t *slot, const int32_t *offsets, void *dx,
-                              cudaStream_t st) {
+                              cudaStream_t st, const RouteNoise *jitter) {
   if (S == 0) return cudaSuccess;
   const dim3 grid((d + kDxC - 1) / kDxC, unsigned((S + kDxT - 1) / kDxT));
+  const RouteNoise nz = jitter ? *jitter : RouteNoise{};
+  const int jit = jitter ? 1 : 0;
   if (dtype == MOE_F32)
     return launch_k(dx_combine_tile_kernel<float>, grid, kDxThreads, 0, st,
                     static_cast<const float *>(dx_disp), dlogits, static_cast<const float *>(w_gate),
-                    S, d, E, k, idx, slot, offsets, static_cast<float *>(dx));
+                    S, d, E, k, idx, slot, offsets, static_cast<float *>(dx), jit, nz);
   return launch_k(dx_combine_tile_kernel<__nv_bfloat16>, grid, kDxThreads, 0, st,
                   static_cast<const __nv_bfloat16 *>(dx_disp), dlogits,
                   static_cast<const __nv_bfloat16 *>(w_gate), S, d, E, k, idx, slot, offsets,
-                  static_cast<__nv_bfloat16 *>(dx));
+                  static_cast<__nv_bfloat16 *>(dx), jit, nz);
 }
 
 }  // namespace moe

@@ -9,6 +9,8 @@
 
 #include <mutex>
 
+#include "moe_b300.h"
+
 namespace moe {
 
 constexpr int kMaxDevices = 64;
@@ -57,6 +59,20 @@ bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t ou
                    uint32_t box_inner, uint32_t box_outer);
 
 // ---------------------------------------------------------------- routing
+// In-layer randomness of the gate (see rng.cuh): the noise policy, the
+// second-choice sampling and random token selection, and the Philox key.
+struct RouteNoise {
+  int policy;        // MOE_NOISE_*
+  int second;        // sampled second choice (k = 2)
+  int rts;           // random token selection
+  float jitter_eps;
+  uint64_t seed, offset;
+  __host__ __device__ bool any() const { return policy != 0 || second != 0 || rts != 0; }
+  __host__ __device__ bool gumbel(int k) const {
+    return policy == MOE_NOISE_RSAMPLE || (second != 0 && k == 2);
+  }
+};
+
 struct RouteArgs {
   const float *logits;  // [S,E] fp32 (bias included)
   int64_t S;
@@ -71,6 +87,7 @@ struct RouteArgs {
   int32_t *routed, *kept, *offsets;  // [E], [E], [E+1]
   int32_t *row_src;     // [rows]
   float *l_aux;
+  RouteNoise noise;      // zero: plain top-k in token order
   // workspace views
   int32_t *hist;        // [nblk][k][E] per-CTA counts, then their scan
   float *psum;          // [nblk][E] per-CTA probability sums
@@ -243,12 +260,22 @@ int64_t gate_wgrad_splits(int64_t S);
 size_t gate_wgrad_partial_bytes(int64_t S, int E, int d);
 cudaError_t launch_gate_wgrad(const float *dlogits, const void *x, int dtype, int64_t S, int d,
                               int E, float *partial, void *dw_gate, cudaStream_t st);
-// dx[s] = sum_j dx_disp[row(s,j)] + dlogits[s] . w_gate
+// dx[s] = sum_j dx_disp[row(s,j)] + (dlogits[s] . w_gate) (* f[s] when
+// `jitter` is set: the router saw x * f)
 cudaError_t launch_dx_combine(const void *dx_disp, const float *dlogits,
                               const void *w_gate, int dtype, int64_t S, int d,
                               int E, int k, const int32_t *idx,
                               const int32_t *slot, const int32_t *offsets,
-                              void *dx, cudaStream_t st);
+                              void *dx, cudaStream_t st, const RouteNoise *jitter = nullptr);
+
+// The gate's draws for a configuration (moe_gate_noise): uniforms and
+// Gumbel noise [S,E], random-token-selection positions [S]; each nullable.
+cudaError_t launch_gate_noise(int64_t S, int E, const RouteNoise &n, float *uniform,
+                              float *gumbel, int32_t *position, cudaStream_t st);
+// The jittered router input xj = x * f (float32 product, rounded to the
+// layer type), [S,d].
+cudaError_t launch_jitter(const void *x, int dtype, int64_t S, int d, const RouteNoise &n,
+                          void *xj, cudaStream_t st);
 
 int num_sms();
 

@@ -21,8 +21,13 @@
 //  3. route_assign: slot = (first-choice total of e if j == 1) + scanned
 //     base + CTA rank.  Every first choice therefore precedes every second
 //     choice, each in token order.  slot >= C -> -1; row_src of kept rows.
+// The randomised gate options (rng.cuh) enter here: step 1 chooses on the
+// logits plus Gumbel noise (rsample, second-choice sampling), and under
+// random token selection the CTAs take the tokens in the order of a keyed
+// permutation, so every "token order" above becomes that queue order.
 #include "common.cuh"
 #include "kernels.h"
+#include "rng.cuh"
 
 namespace moe {
 namespace {
@@ -33,11 +38,15 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Under random token selection (noise.rts) CTA b works on the tokens at
+// queue positions b*kTB ... b*kTB + kTB - 1 instead of those token indices,
+// so counts and ranks come out in queue order; every per-token output is
+// still written at the token's own index.
 __global__ void __launch_bounds__(kTB)
 route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, float inv_temp,
                   float *__restrict__ probs, int32_t *__restrict__ idx_out,
                   float *__restrict__ w_out, int32_t *__restrict__ rank_out,
-                  int32_t *__restrict__ hist, float *__restrict__ psum) {
+                  int32_t *__restrict__ hist, float *__restrict__ psum, RouteNoise noise) {
   griddep_begin();
   __shared__ int32_t s_choice[2][kTB];
   __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
@@ -46,6 +55,10 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t tok0 = int64_t(blockIdx.x) * kTB;
   const int nq = (E + 31) >> 5;
+  const rng::Key key = rng::make_key(noise.seed, noise.offset);
+  const rng::Perm perm = rng::make_perm(key, uint32_t(S));
+  const bool use_gumbel = noise.gumbel(k);
+  const bool sample_all = noise.policy == MOE_NOISE_RSAMPLE;
 
   float pacc[kMaxPerLane];
 #pragma unroll
@@ -53,22 +66,28 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
 
   // ---- phase 1: one warp per token, lanes over experts
   for (int t = warp; t < kTB; t += kWarps) {
-    const int64_t s = tok0 + t;
-    if (s >= S) {
+    if (tok0 + t >= S) {
       if (lane == 0) {
         s_choice[0][t] = -1;
         s_choice[1][t] = -1;
       }
       continue;
     }
+    const int64_t s = noise.rts ? int64_t(rng::token_at(perm, uint32_t(tok0 + t))) : tok0 + t;
     const float *row = logits + s * E;
-    float v[kMaxPerLane];
+    float v[kMaxPerLane], key_v[kMaxPerLane];
     float m = -INFINITY;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
       const int e = lane + 32 * q;
       v[q] = (q < nq && e < E) ? row[e] : -INFINITY;
       m = fmaxf(m, v[q]);
+      key_v[q] = v[q];
+      if (use_gumbel && q < nq && e < E) {
+        // the selection key: logit + Gumbel noise, one float32 addition
+        const uint4 w4 = rng::block(key, rng::kPurposeGateNoise, uint32_t(s), uint32_t(e >> 2));
+        key_v[q] = __fadd_rn(v[q], rng::gumbel(rng::uniform(rng::word(w4, e & 3))));
+      }
     }
     m = warp_max(m);
     float ex[kMaxPerLane];
@@ -81,26 +100,30 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
     }
     z = warp_sum(z);
     const float inv_z = 1.0f / z;
-    // top-1 (ties -> lower index)
+    // top-1 (ties -> lower index), on the noisy keys under rsample
     float b1 = -INFINITY;
     int i1 = -1;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
       const int e = lane + 32 * q;
-      if (q < nq && e < E && (i1 < 0 || v[q] > b1)) {
-        b1 = v[q];
+      const float c = sample_all ? key_v[q] : v[q];
+      if (q < nq && e < E && (i1 < 0 || c > b1)) {
+        b1 = c;
         i1 = e;
       }
     }
     warp_argmax(b1, i1);
     int i2 = -1;
     if (k == 2) {
+      // the second choice: on the noisy keys under rsample or second-choice
+      // sampling
       float b2 = -INFINITY;
 #pragma unroll
       for (int q = 0; q < kMaxPerLane; ++q) {
         const int e = lane + 32 * q;
-        if (q < nq && e < E && e != i1 && (i2 < 0 || v[q] > b2)) {
-          b2 = v[q];
+        const float c = use_gumbel ? key_v[q] : v[q];
+        if (q < nq && e < E && e != i1 && (i2 < 0 || c > b2)) {
+          b2 = c;
           i2 = e;
         }
       }
@@ -153,9 +176,10 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
     psum[int64_t(blockIdx.x) * E + e] = acc;
   }
 
-  // ---- phase 2: one lane per token; rank among equal (j, e) in token order
+  // ---- phase 2: one lane per token; rank among equal (j, e) in queue order
   const int t = threadIdx.x;
-  const int64_t s = tok0 + t;
+  const int64_t s = (noise.rts && tok0 + t < S) ? int64_t(rng::token_at(perm, uint32_t(tok0 + t)))
+                                                 : tok0 + t;
   for (int j = 0; j < k; ++j) {
     for (int i = threadIdx.x; i < kWarps * kMaxExperts; i += kTB) (&s_wcnt[0][0])[i] = 0;
     block_sync();
@@ -312,14 +336,20 @@ __global__ void route_assign_kernel(int64_t S, int E, int k, int64_t cap, int64_
                                     const int32_t *__restrict__ first_cnt,
                                     const int32_t *__restrict__ offsets,
                                     int32_t *__restrict__ slot,
-                                    int32_t *__restrict__ row_src) {
+                                    int32_t *__restrict__ row_src, RouteNoise noise) {
   griddep_begin();
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= S * k) return;
   const int64_t s = i / k;
   const int j = int(i - s * k);
   const int e = idx[i];
-  const int64_t b = s / kTB;
+  // the CTA that ranked this token: by token index, or by queue position
+  const int64_t b =
+      (noise.rts ? int64_t(rng::position_of(
+                       rng::make_perm(rng::make_key(noise.seed, noise.offset), uint32_t(S)),
+                       uint32_t(s)))
+                 : s) /
+      kTB;
   const int pos = hist[(b * k + j) * E + e] + (j == 1 ? first_cnt[e] : 0) + slot[i];
   if (cap < 0 || pos < cap) {
     slot[i] = pos;
@@ -357,10 +387,77 @@ cudaError_t launch_route_finish(const RouteArgs &a, cudaStream_t st) {
   if (n > 0) {
     if (const cudaError_t e = launch_k(route_assign_kernel, unsigned((n + 255) / 256), 256, 0, st,
                                        a.S, a.E, a.k, a.cap, nblk, a.idx, a.hist, a.first_cnt,
-                                       a.offsets, a.slot, a.row_src); e != cudaSuccess)
+                                       a.offsets, a.slot, a.row_src, a.noise); e != cudaSuccess)
       return e;
   }
   return cudaGetLastError();
+}
+
+namespace {
+
+// one thread per token: uniforms / Gumbel noise of its experts and its
+// queue position
+__global__ void gate_noise_kernel(int64_t S, int E, RouteNoise noise, float *__restrict__ uniform,
+                                  float *__restrict__ gumbel, int32_t *__restrict__ position) {
+  griddep_begin();
+  const int64_t s = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  const rng::Key key = rng::make_key(noise.seed, noise.offset);
+  if (position) position[s] = int32_t(rng::position_of(rng::make_perm(key, uint32_t(S)), uint32_t(s)));
+  for (int e4 = 0; e4 < E; e4 += 4) {
+    const uint4 w4 = rng::block(key, rng::kPurposeGateNoise, uint32_t(s), uint32_t(e4 >> 2));
+    for (int i = 0; i < 4 && e4 + i < E; ++i) {
+      const float u = rng::uniform(rng::word(w4, i));
+      if (uniform) uniform[s * E + e4 + i] = u;
+      if (gumbel) gumbel[s * E + e4 + i] = rng::gumbel(u);
+    }
+  }
+}
+
+// xj[s, c] = x[s, c] * f[s, c], eight elements per thread (two Philox blocks)
+template <typename T>
+__global__ void jitter_kernel(const T *__restrict__ x, int64_t S, int d, RouteNoise noise,
+                              T *__restrict__ xj) {
+  griddep_begin();
+  const int n8 = d / 8;
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= S * n8) return;
+  const int64_t s = i / n8;
+  const int c0 = int(i - s * n8) * 8;
+  const rng::Key key = rng::make_key(noise.seed, noise.offset);
+  const float eps = noise.jitter_eps > 0.0f ? noise.jitter_eps : 0.01f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 w4 = rng::block(key, rng::kPurposeJitter, uint32_t(s), uint32_t((c0 >> 2) + h));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t o = s * d + c0 + h * 4 + q;
+      const float f = rng::jitter(rng::uniform(rng::word(w4, q)), eps);
+      xj[o] = T(__fmul_rn(float(x[o]), f));
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gate_noise(int64_t S, int E, const RouteNoise &n, float *uniform,
+                              float *gumbel, int32_t *position, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  return launch_k(gate_noise_kernel, unsigned((S + 127) / 128), 128, 0, st, S, E, n, uniform,
+                  gumbel, position);
+}
+
+cudaError_t launch_jitter(const void *x, int dtype, int64_t S, int d, const RouteNoise &n,
+                          void *xj, cudaStream_t st) {
+  const int64_t total = S * (d / 8);
+  if (total == 0) return cudaSuccess;
+  const unsigned grid = unsigned((total + 255) / 256);
+  if (dtype == MOE_F32)
+    return launch_k(jitter_kernel<float>, grid, 256, 0, st, static_cast<const float *>(x), S, d,
+                    n, static_cast<float *>(xj));
+  return launch_k(jitter_kernel<__nv_bfloat16>, grid, 256, 0, st,
+                  static_cast<const __nv_bfloat16 *>(x), S, d, n,
+                  static_cast<__nv_bfloat16 *>(xj));
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
@@ -368,7 +465,7 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st) {
   if (nblk > 0) {
     if (const cudaError_t e = launch_k(route_topk_kernel, unsigned(nblk), kTB, 0, st, a.logits, a.S,
                                        a.E, a.k, a.inv_temp, a.probs, a.idx, a.w, a.slot,
-                                       a.hist, a.psum); e != cudaSuccess)
+                                       a.hist, a.psum, a.noise); e != cudaSuccess)
       return e;
   }
   const cudaError_t e = cudaGetLastError();

@@ -49,6 +49,12 @@ class Workload:
     gate_temperature: float = 1.0   # softmax temperature of the gate
     aux_loss_type: str = "load"     # "load" | "std"
     logit_noise_std: float = 0.0    # > 0: per-token gate noise N(0, std^2), [S, E]
+    noise_policy: str = "none"      # in-layer gate noise: "none" | "jitter" | "rsample"
+    second_expert_sampling: bool = False
+    use_rts: bool = False           # random token selection
+    jitter_eps: float = 0.01
+    noise_seed: int = 0
+    noise_offset: int = 0
 
     def scaled(self, num_tokens: int, **kw) -> "Workload":
         """Same layer shape and routing settings with a different batch."""

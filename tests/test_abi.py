@@ -177,3 +177,22 @@ def test_fused_dispatch_argument_checks():
     nodisp.x_disp = None
     assert lib.moe_forward(ctypes.byref(f32), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
                            ctypes.byref(nodisp), FAKE, 1 << 40, None) == N.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [dict(noise_policy=3), dict(noise_policy=-1),
+                                 dict(second_expert_sampling=2), dict(use_rts=5),
+                                 dict(jitter_eps=-0.1), dict(jitter_eps=1.0)])
+def test_invalid_noise_options_rejected(bad):
+    cfg = N.make_config(64, 32, 64, 4, 2, 1.0, 4, True, "relu", "f32")
+    for k, v in bad.items():
+        setattr(cfg, k, v)
+    rows = ctypes.c_int64()
+    assert N.library().moe_max_rows(ctypes.byref(cfg), ctypes.byref(rows)) == N.MOE_ERR_INVALID_ARG
+
+
+def test_noise_workspace_holds_the_jittered_input():
+    base = N.make_config(4096, 512, 64, 8, 2, 1.0, 4, True)
+    jit = N.make_config(4096, 512, 64, 8, 2, 1.0, 4, True, noise_policy="jitter")
+    extra = N.moe_workspace_size(jit) - N.moe_workspace_size(base)
+    assert extra >= 4096 * 512 * 2
+    assert N.moe_workspace_size(jit, True) - N.moe_workspace_size(base, True) >= 4096 * 512 * 2
