@@ -345,6 +345,15 @@ moe_status moe_backward(const moe_config *cfg, const void *x,
                         void *db2, void *workspace, size_t workspace_bytes,
                         moe_stream_t stream);
 
+/* Debugging aid: the time limit, on the current device, of the waits of
+ * the single-launch bf16 gate kernel that follow its progress (a copy, an
+ * MMA, the grid-wide barrier); ns = 0 restores the default of 2 s.  A
+ * limit short enough to run out makes the kernel give up, record its code in
+ * the device error word (moe_get_device_error), drain its own copies and
+ * MMAs and return, leaving its outputs unspecified but in range; the next
+ * call with the default limit computes normally.  Synchronous. */
+moe_status moe_debug_set_wait_limit(uint64_t ns);
+
 /* Reads and clears the device error word on the current device
  * (synchronous).  *code == 0 means no kernel recorded a fault; otherwise it
  * names the kernel and wait that gave up.  Returns MOE_ERR_DEVICE when

@@ -75,6 +75,7 @@ _SIGS = {
     "moe_backward": (c_int, [POINTER(MoeConfig)] + [_P] * 4 + [POINTER(MoeBuffers)] + [_P] * 8
                      + [c_size_t, _P]),
     "moe_get_device_error": (c_int, [POINTER(c_uint32)]),
+    "moe_debug_set_wait_limit": (c_int, [ctypes.c_uint64]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -261,6 +262,11 @@ def moe_backward(cfg, x, w_gate, w1, w2, saved, dy, dx, dw_gate, dw1, db1, dw2, 
         ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(w1), _ptr(w2), ctypes.byref(b), _ptr(dy),
         _ptr(dx), _ptr(dw_gate), _ptr(dw1), _ptr(db1), _ptr(dw2), _ptr(db2), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_debug_set_wait_limit(ns: int):
+    """Progress-wait limit of the single-launch gate kernel (0: 2 s)."""
+    _check("moe_debug_set_wait_limit", _lib.moe_debug_set_wait_limit(int(ns)))
 
 
 def moe_get_device_error() -> int:

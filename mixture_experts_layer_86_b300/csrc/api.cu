@@ -675,6 +675,10 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
                                        noise.policy == MOE_NOISE_JITTER ? &noise : nullptr));
 }
 
+moe_status moe_debug_set_wait_limit(uint64_t ns) {
+  return cuda_status(set_gate_wait_limit(ns));
+}
+
 moe_status moe_get_device_error(uint32_t *code) {
   if (!code) return MOE_ERR_INVALID_ARG;
   unsigned int *p = device_error_ptr();

@@ -61,6 +61,13 @@ struct GridBarrierWords {
 constexpr int kGateBarrierSlots = 64;
 __device__ GridBarrierWords g_gate_barrier[kGateBarrierSlots];
 
+// Time limit of the waits that follow the kernel's progress (for a copy, an
+// MMA, the grid barrier).  2 s unless moe_debug_set_wait_limit changed it to
+// exercise the give-up path.  The waits that drain this CTA's own copies and
+// MMAs before it exits keep their fixed limit, so no copy or MMA is still in
+// flight when the CTA leaves.
+__device__ unsigned long long g_gate_wait_limit_ns = 2000000000ull;
+
 namespace {
 
 constexpr int kGrThreads = 256;                 // 8 warps
@@ -167,6 +174,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   const int64_t tok0 = int64_t(tile) * p.TM;
   const int E = p.E, k = p.k;
   const uint32_t wbox_bytes = uint32_t(p.E_pad) * 128;
+  const uint64_t lim = g_gate_wait_limit_ns;
 
   // ---------------------------------------------------------------- setup
   if (tid == 0) {
@@ -216,7 +224,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       for (int kb = 0; kb < p.nk; ++kb) {
         const int stage = kb % p.nstages;
         const uint32_t phase = (kb / p.nstages) & 1;
-        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kGrWaitNs)) {
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, lim)) {
           record_error(p.err, kErrGateProducer | uint32_t(tile & 0xffffff));
           *abort = 1;
           ok = false;
@@ -248,7 +256,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       for (int kb = 0; kb < p.nk; ++kb) {
         const int stage = kb % p.nstages;
         const uint32_t phase = (kb / p.nstages) & 1;
-        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kGrWaitNs)) {
+        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, lim)) {
           record_error(p.err, kErrGateMma | uint32_t(tile & 0xffffff));
           *abort = 1;
           ok = false;
@@ -277,7 +285,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int r = q * 32 + lane;
     const int64_t s = tok0 + r;
     const bool valid = r < p.TM && s < p.S;
-    if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, kGrWaitNs)) {
+    if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, lim)) {
       record_error(p.err, kErrGateEpilogue | uint32_t(tile & 0xffffff));
       *abort = 1;
     }
@@ -424,7 +432,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
 
   // ------------------------------------------------------- grid barrier
   if (tid == 0) {
-    const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles), kGrWaitNs);
+    const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles), lim);
     if (!ok) record_error(p.err, kErrGateBarrier | uint32_t(tile & 0xffffff));
     ctl.barrier_ok = ok ? 1 : 0;
   }
@@ -591,6 +599,11 @@ unsigned int next_barrier_slot() {
 }
 
 }  // namespace
+
+cudaError_t set_gate_wait_limit(uint64_t ns) {
+  const unsigned long long v = ns ? ns : 2000000000ull;
+  return cudaMemcpyToSymbol(g_gate_wait_limit_ns, &v, sizeof(v));
+}
 
 cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   if (a.S <= 0) return cudaErrorNotSupported;

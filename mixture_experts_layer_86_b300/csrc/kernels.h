@@ -144,6 +144,9 @@ struct GateRouteArgs {
   unsigned int *err;
 };
 cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st);
+// The single-launch gate's progress-wait limit on the current device
+// (0: the default 2 s); synchronous.
+cudaError_t set_gate_wait_limit(uint64_t ns);
 
 // ------------------------------------------------------ SIMT grouped GEMM
 // C(m,n) = epilogue( sum_k A(m,k) * B(n,k) ) with arbitrary element strides.
