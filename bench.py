@@ -106,58 +106,125 @@ def forward_launches(wl, fused: bool, num_sms: int) -> int:
 
 
 # ------------------------------------------------------------------ clocks
+class _NvmlCtypes:
+    """The few read-only NVML queries the sampler needs, straight from
+    libnvidia-ml through ctypes (for hosts without the pynvml module)."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.handle = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+        except Exception:  # noqa: BLE001
+            bus = None
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.handle)):
+            if lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                raise RuntimeError("no NVML handle")
+        try:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _u32(self, fn, *args):
+        v = self.ct.c_uint()
+        if fn(self.handle, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def sm(self):
+        return float(self._u32(self.lib.nvmlDeviceGetClockInfo, self.NVML_CLOCK_SM))
+
+    def sm_max(self):
+        return float(self._u32(self.lib.nvmlDeviceGetMaxClockInfo, self.NVML_CLOCK_SM))
+
+    def power_w(self):
+        return self._u32(self.lib.nvmlDeviceGetPowerUsage) / 1000.0
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        if self._reasons_fn(self.handle, self.ct.byref(v)) != 0:
+            raise RuntimeError("clock event reasons")
+        return int(v.value)
+
+
+class _NvmlPy:
+    """The same queries through the pynvml module."""
+
+    def __init__(self, index: int):
+        import pynvml
+        pynvml.nvmlInit()
+        self.n = pynvml
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+            self.handle = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:  # noqa: BLE001
+            self.handle = pynvml.nvmlDeviceGetHandleByIndex(index)
+
+    def sm(self):
+        return float(self.n.nvmlDeviceGetClockInfo(self.handle, self.n.NVML_CLOCK_SM))
+
+    def sm_max(self):
+        return float(self.n.nvmlDeviceGetMaxClockInfo(self.handle, self.n.NVML_CLOCK_SM))
+
+    def power_w(self):
+        return self.n.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
+
+    def reasons(self):
+        try:
+            return int(self.n.nvmlDeviceGetCurrentClocksEventReasons(self.handle))
+        except Exception:  # noqa: BLE001
+            return int(self.n.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle))
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons of one GPU, polled from a
-    background thread while the timed region runs (read-only NVML queries;
-    nvidia-smi at its fastest interval when NVML is not importable)."""
+    background thread while the timed region runs (read-only NVML queries,
+    through pynvml or directly through libnvidia-ml; one nvidia-smi reading
+    after the region when neither works)."""
 
     REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
                ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
 
-    def __init__(self, device_index: int, interval_s: float = 0.0005):
+    def __init__(self, device_index: int, interval_s: float = 0.0002):
         self.index = device_index
         self.interval = interval_s
         self.rows = []
         self.stop_evt = threading.Event()
         self.thread = None
-        self.handle = None
         self.nvml = None
         self.source = "none"
         self.nvml_error = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.handle = self._handle(pynvml)
-            self.sm_max = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
-            self.nvml = pynvml
-            self.source = "nvml"
-        except Exception as e:  # noqa: BLE001  (reported in the clocks record)
-            self.nvml = None
-            self.nvml_error = f"{type(e).__name__}: {e}"
-
-    def _handle(self, pynvml):
-        try:
-            import torch
-            p = torch.cuda.get_device_properties(self.index)
-            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
-            return pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-        except Exception:
-            return pynvml.nvmlDeviceGetHandleByIndex(self.index)
-
-    def _reasons(self):
-        try:
-            return self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle)
-        except Exception:
-            return self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons(self.handle)
+        errors = []
+        for name, cls in (("nvml (pynvml)", _NvmlPy), ("nvml (libnvidia-ml via ctypes)", _NvmlCtypes)):
+            try:
+                backend = cls(device_index)
+                self.sm_max = backend.sm_max()
+                backend.sm()
+                backend.reasons()
+                self.nvml, self.source = backend, name
+                break
+            except Exception as e:  # noqa: BLE001  (reported in the clocks record)
+                errors.append(f"{name}: {type(e).__name__}: {e}")
+        if self.nvml is None:
+            self.nvml_error = "; ".join(errors)
 
     def _poll(self):
         n = self.nvml
         while not self.stop_evt.is_set():
             try:
-                sm = float(n.nvmlDeviceGetClockInfo(self.handle, n.NVML_CLOCK_SM))
-                pw = n.nvmlDeviceGetPowerUsage(self.handle) / 1000.0
-                self.rows.append((sm, pw, int(self._reasons())))
-            except Exception:
+                self.rows.append((n.sm(), n.power_w(), n.reasons()))
+            except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.interval)
 
@@ -233,10 +300,9 @@ STAGES = ("gate", "dispatch", "expert_ffn", "combine")
 class LayerRun:
     """Device state of one workload (inputs, buffers, workspaces) and its
     stage calls through the C ABI.  The forward runs the stage entry points,
-    the kernels moe_forward launches in its order: for a bf16 forward without
-    a backward, the dispatch is fused into the first expert GEMM
-    (moe_expert_ffn_gather, no x_disp copy), else moe_dispatch then
-    moe_expert_ffn."""
+    the kernels moe_forward launches in its order: moe_dispatch then
+    moe_expert_ffn, or with fused=True the expert FFN reading the token rows
+    straight from x (moe_expert_ffn_gather, no x_disp copy)."""
 
     def __init__(self, wl, dev, fused=None):
         import torch
@@ -250,7 +316,7 @@ class LayerRun:
         self.inp_cpu = make_inputs(wl)
         self.d = self.inp_cpu.to(dev)
         self.train = wl.backward
-        self.fused = (wl.dtype == "bf16" and not self.train) if fused is None else fused
+        self.fused = False if fused is None else fused
         self.names = (("gate", "expert_ffn", "combine") if self.fused else STAGES) + \
             (("backward",) if self.train else ())
         self.bufs = L.alloc_buffers(self.cfg, dev, training=self.train,
@@ -455,11 +521,11 @@ def run_gpu(args):
     # moe_forward with an x_disp buffer (the dispatch as its own copy kernel)
     fwd_call_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
         cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, run.bufs, run.ws, st)))
-    bufs_copy = L.alloc_buffers(cfg, dev)
-    bufs_copy["logits"] = None
-    copy_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
-        cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, bufs_copy, run.ws, st)))
-    del bufs_copy
+    bufs_fused = L.alloc_buffers(cfg, dev, fused_dispatch=True)
+    bufs_fused["logits"] = None
+    fused_ms = max_over_ranks(timed(torch, st, args.steps, lambda i: N.moe_forward(
+        cfg, d.x, d.w_gate, d.logit_bias, d.w1, d.b1, d.w2, d.b2, run.y, bufs_fused, run.ws, st)))
+    del bufs_fused
     stages = stage_breakdown(run, st, args.steps, peaks)
     cold = stages_cold_l2(run, st, peaks)
     rstats = routing_stats(run)
@@ -566,7 +632,7 @@ def run_gpu(args):
                 "timing": "CUDA events: before the first host-to-device copy, after the last "
                           "device-to-host copy"},
         "moe_forward_ms_per_step": fwd_call_ms / args.steps,
-        "moe_forward_with_dispatch_copy_ms_per_step": copy_ms / args.steps,
+        "moe_forward_fused_dispatch_ms_per_step": fused_ms / args.steps,
         "dispatch": "fused into the first expert GEMM" if run_fused else "copy kernel",
         "gpu_launches": forward_launches(wl, run_fused, num_sms) * args.steps,
         "clocks": clocks,
@@ -624,7 +690,7 @@ def residual_step(args, dev, run, max_over_ranks, world):
     wl, cfg, d = run.wl, run.cfg, run.d
     rw = [t.to(dev) for t in make_residual_weights(wl)]
     mix_w, mix_b = [t.to(dev) for t in make_residual_mix(wl)]
-    bufs = L.alloc_buffers(cfg, dev, fused_dispatch=wl.dtype == "bf16")
+    bufs = L.alloc_buffers(cfg, dev)
     bufs["logits"] = None
     ws = L.alloc_workspace(cfg, dev)
     y = torch.empty_like(d.x)

@@ -96,6 +96,9 @@ struct __align__(16) GrCtl {
   int32_t offs[kMaxExperts + 1];    // expert offsets
   int32_t choice[2][kGrMaxTile];    // chosen expert per (j, token), -1 none
   int32_t rank[2][kGrMaxTile];      // rank among the tile's (j, e) tokens
+  float cand_v[2][kGrMaxTile][2];   // each half's top-2 logits per token
+  int32_t cand_i[2][kGrMaxTile][2]; // and their experts
+  float zpart[2][kGrMaxTile];       // each half's softmax sum per token
   long long aux[kMaxExperts];       // sum over tokens of p[., e], 2^-30 units
 };
 
@@ -118,6 +121,7 @@ struct GrParams {
   int32_t *hist;        // [ntiles][hist_pitch] counts per (j, e)
   float *psum;          // [ntiles][psum_pitch] probability sums per e
   int hist_pitch, psum_pitch;
+  int chunks_per_warp;  // 32-expert chunks each epilogue warp keeps in shared memory
   unsigned int *err;
   unsigned int barrier_slot;
 };
@@ -279,10 +283,20 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // after a give-up, the MMAs already issued finish before TMEM is freed
       if (!ok) ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, nullptr, kGrWaitNs / 4);
     }
-  } else if (warp >= 4) {
-    // -------------------------------------------- epilogue: lane = token
-    const int q = warp & 3;  // TMEM lane quadrant this warp may read
-    const int r = q * 32 + lane;
+  }
+
+  // ---------------------------------------------- epilogue: all 8 warps
+  // Warp w reads TMEM lane quadrant q = w % 4 (tokens 32q .. 32q+31 of the
+  // tile) and the expert chunks c = h, h + 2, ... (h = w / 4) of 32 experts
+  // each.  Per chunk the logits (+ bias) go to a 32 x 33 shared tile, whose
+  // rows are tokens and columns experts, so that logits, then exp(l - m),
+  // then probabilities live in the same tile; the two warps of a quadrant
+  // merge their top-2 candidates, maxima and sums through shared memory in a
+  // fixed order.  The ring is idle once every MMA is done.
+  __syncwarp();
+  {
+    const int q = warp & 3, h = warp >> 2;
+    const int r = q * 32 + lane;  // token row of the tile
     const int64_t s = tok0 + r;
     const bool valid = r < p.TM && s < p.S;
     if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, lim)) {
@@ -290,23 +304,24 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       *abort = 1;
     }
     ptx::tc_fence_after();
-    // the ring is idle once every MMA is done: each warp's transpose tile
-    float *stg = reinterpret_cast<float *>(ring) + q * kStgFloats;
     const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
     const float *brow = (p.logit_bias != nullptr && p.bias_ld != 0 && valid)
                             ? p.logit_bias + s * p.bias_ld
                             : nullptr;
     const int nchunk = (E + 31) >> 5;
+    const int my_chunks = (nchunk - h + 1) >> 1;  // chunks h, h+2, ...
+    float *stg0 = reinterpret_cast<float *>(ring) + (warp * p.chunks_per_warp) * kStgFloats;
     const int64_t wrow0 = tok0 + q * 32;  // first token of this warp's rows
-    // valid rows of this warp (<= 0 when the warp's lanes are all past the tile)
-    int64_t wr = p.S - wrow0;
+    int64_t wr = p.S - wrow0;              // valid rows of this warp (<= 0: none)
     if (wr > p.TM - q * 32) wr = p.TM - q * 32;
     const int wrows = wr > 32 ? 32 : int(wr);
 
-    // pass 1: top-2 (ties to the lower index) and the optional logits rows
+    // pass 1: logits (+ bias) into the shared tiles; top-2 candidates
     float b1 = -INFINITY, b2 = -INFINITY;
     int i1 = -1, i2 = -1;
-    for (int c = 0; c < nchunk; ++c) {
+    for (int ci = 0; ci < my_chunks; ++ci) {
+      const int c = h + 2 * ci;
+      float *stg = stg0 + ci * kStgFloats;
       uint32_t raw[32];
       ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
       ptx::tmem_ld_wait();
@@ -324,47 +339,71 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
             b2 = v;
             i2 = e;
           }
-          if (p.logits) stg[lane * 33 + t] = v;
+          stg[lane * 33 + t] = v;
         }
       }
-      if (p.logits) {
+      if (p.logits) {  // coalesced rows of the logits
         __syncwarp();
         const int e = c * 32 + lane;
         for (int rr = 0; rr < wrows; ++rr)
           if (e < E) p.logits[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
-        __syncwarp();
       }
     }
-    // pass 2: the softmax normaliser (the top-1 logit is the shift)
-    const float m = b1;
+    ptx::tc_fence_before();
+    ctl.cand_v[h][r][0] = b1;
+    ctl.cand_v[h][r][1] = b2;
+    ctl.cand_i[h][r][0] = i1;
+    ctl.cand_i[h][r][1] = i2;
+    block_sync();
+    // the row's top-2 over both halves: ranked by value, ties to the lower
+    // expert index (each half's candidates come in that order already)
+    {
+      const float ov1 = ctl.cand_v[h ^ 1][r][0], ov2 = ctl.cand_v[h ^ 1][r][1];
+      const int oi1 = ctl.cand_i[h ^ 1][r][0], oi2 = ctl.cand_i[h ^ 1][r][1];
+      auto before = [](float av, int ai, float bv, int bi) {
+        return ai >= 0 && (bi < 0 || av > bv || (av == bv && ai < bi));
+      };
+      if (before(ov1, oi1, b1, i1)) {
+        if (before(b1, i1, ov2, oi2)) {
+          b2 = b1;
+          i2 = i1;
+        } else {
+          b2 = ov2;
+          i2 = oi2;
+        }
+        b1 = ov1;
+        i1 = oi1;
+      } else if (before(ov1, oi1, b2, i2)) {
+        b2 = ov1;
+        i2 = oi1;
+      }
+    }
+    const float m = b1;  // the top-1 logit is the softmax shift
+    // pass 2: exp((l - m) / T) in place; this half's sum
     float z = 0.0f;
-    for (int c = 0; c < nchunk; ++c) {
-      uint32_t raw[32];
-      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
-      ptx::tmem_ld_wait();
+    for (int ci = 0; ci < my_chunks; ++ci) {
+      const int c = h + 2 * ci;
+      float *stg = stg0 + ci * kStgFloats;
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
-        const int e = c * 32 + t;
-        if (e < E)
-          z += expf((__uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]) - m) * p.inv_temp);
+        if (c * 32 + t < E) {
+          const float ev = expf((stg[lane * 33 + t] - m) * p.inv_temp);
+          stg[lane * 33 + t] = ev;
+          z += ev;
+        }
       }
     }
-    const float inv_z = 1.0f / z;
-    // pass 3: probabilities (0 for rows past the batch), the tile's column
-    // sums and the optional probability rows
-    for (int c = 0; c < nchunk; ++c) {
-      uint32_t raw[32];
-      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
-      ptx::tmem_ld_wait();
+    ctl.zpart[h][r] = z;
+    block_sync();
+    const float inv_z = 1.0f / (ctl.zpart[0][r] + ctl.zpart[1][r]);
+    // pass 3: probabilities (0 past the batch), column sums over the tile's
+    // rows in a fixed order, the optional probability rows
+    for (int ci = 0; ci < my_chunks; ++ci) {
+      const int c = h + 2 * ci;
+      float *stg = stg0 + ci * kStgFloats;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const int e = c * 32 + t;
-        float pv = 0.0f;
-        if (e < E && valid)
-          pv = expf((__uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]) - m) * p.inv_temp) *
-               inv_z;
-        stg[lane * 33 + t] = pv;
-      }
+      for (int t = 0; t < 32; ++t)
+        if (c * 32 + t < E) stg[lane * 33 + t] = valid ? stg[lane * 33 + t] * inv_z : 0.0f;
       __syncwarp();
       const int e = c * 32 + lane;
       float cs = 0.0f;
@@ -375,23 +414,29 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
           if (e < E) p.probs[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
       __syncwarp();
     }
-    ptx::tc_fence_before();
-    if (valid) {
-      p.idx[s * k] = i1;
-      if (k == 1) {
-        p.w[s] = inv_z;  // exp(l1 - max) = 1
-      } else {
-        const float x2 = expf((b2 - m) * p.inv_temp);
-        const float den = 1.0f + x2;
-        p.w[s * 2] = 1.0f / den;
-        p.w[s * 2 + 1] = x2 / den;
-        p.idx[s * 2 + 1] = i2;
+    if (h == 0) {
+      if (valid) {
+        p.idx[s * k] = i1;
+        if (k == 1) {
+          p.w[s] = inv_z;  // exp(l1 - max) = 1
+        } else {
+          const float x2 = expf((b2 - m) * p.inv_temp);
+          const float den = 1.0f + x2;
+          p.w[s * 2] = 1.0f / den;
+          p.w[s * 2 + 1] = x2 / den;
+          p.idx[s * 2 + 1] = i2;
+        }
       }
+      ctl.choice[0][r] = valid ? i1 : -1;
+      ctl.choice[1][r] = (valid && k == 2) ? i2 : -1;
     }
-    ctl.choice[0][r] = valid ? i1 : -1;
-    ctl.choice[1][r] = (valid && k == 2) ? i2 : -1;
+  }
+  block_sync();
 
+  if (warp >= 4) {
     // the tile's count and each token's rank per (j, e), in token order
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
     const int et = tid - 128;  // 0..127 over warps 4..7
     for (int j = 0; j < k; ++j) {
       for (int i = et; i < 4 * kMaxExperts; i += 128) (&ctl.wcnt[0][0])[i] = 0;
@@ -414,14 +459,17 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       ctl.rank[j][r] = e >= 0 ? ctl.wcnt[q][e] + rk : 0;
       epi_sync();
     }
-    // publish the tile's counts and probability sums (padding entries 0)
-    for (int i = et; i < p.hist_pitch; i += 128)
-      p.hist[int64_t(tile) * p.hist_pitch + i] = i < k * E ? ctl.cnt[i / E][i % E] : 0;
-    for (int e = et; e < p.psum_pitch; e += 128)
+  } else {
+    // publish the tile's probability sums (padding entries 0)
+    for (int e = tid; e < p.psum_pitch; e += 128)
       p.psum[int64_t(tile) * p.psum_pitch + e] =
           e < E ? ((ctl.psum_w[0][e] + ctl.psum_w[1][e]) + ctl.psum_w[2][e]) + ctl.psum_w[3][e]
                 : 0.0f;
   }
+  block_sync();
+  // publish the tile's counts (padding entries 0)
+  for (int i = tid; i < p.hist_pitch; i += kGrThreads)
+    p.hist[int64_t(tile) * p.hist_pitch + i] = i < k * E ? ctl.cnt[i / E][i % E] : 0;
 
   ptx::tc_fence_before();
   block_sync();
@@ -450,22 +498,21 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
     const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
     if (g < RG && okb) {
-      int t = g;
-      for (; t + 3 * RG < p.ntiles; t += 4 * RG) {
-        const int4 a0 = __ldcg(h4 + int64_t(t) * nv + v);
-        const int4 a1 = __ldcg(h4 + int64_t(t + RG) * nv + v);
-        const int4 a2 = __ldcg(h4 + int64_t(t + 2 * RG) * nv + v);
-        const int4 a3 = __ldcg(h4 + int64_t(t + 3 * RG) * nv + v);
-        tot = add4(add4(tot, a0), add4(a1, add4(a2, a3)));
-        if (t < tile) pre = add4(pre, a0);
-        if (t + RG < tile) pre = add4(pre, a1);
-        if (t + 2 * RG < tile) pre = add4(pre, a2);
-        if (t + 3 * RG < tile) pre = add4(pre, a3);
-      }
-      for (; t < p.ntiles; t += RG) {
-        const int4 a0 = __ldcg(h4 + int64_t(t) * nv + v);
-        tot = add4(tot, a0);
-        if (t < tile) pre = add4(pre, a0);
+      // 16 rows per round, every load issued before any is used: the prefix
+      // costs a round trip to L2 per 16 * RG tiles
+      constexpr int kU = 16;
+      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
+        int4 a[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int t = t0 + u * RG;
+          a[u] = t < p.ntiles ? __ldcg(h4 + int64_t(t) * nv + v) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          tot = add4(tot, a[u]);
+          if (t0 + u * RG < tile) pre = add4(pre, a[u]);
+        }
       }
     }
     int4 *red = reinterpret_cast<int4 *>(ring);  // [2][RG][nv]
@@ -543,14 +590,24 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int v = tid % nv, g = tid / nv;
     long long a[4] = {0, 0, 0, 0};
     const float4 *p4 = reinterpret_cast<const float4 *>(p.psum);
-    if (g < RG && okb)
-      for (int t = g; t < p.ntiles; t += RG) {
-        const float4 f = __ldcg(p4 + int64_t(t) * nv + v);
-        a[0] += __float2ll_rn(f.x * 1073741824.0f);
-        a[1] += __float2ll_rn(f.y * 1073741824.0f);
-        a[2] += __float2ll_rn(f.z * 1073741824.0f);
-        a[3] += __float2ll_rn(f.w * 1073741824.0f);
+    if (g < RG && okb) {
+      constexpr int kU = 16;
+      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
+        float4 f[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int t = t0 + u * RG;
+          f[u] = t < p.ntiles ? __ldcg(p4 + int64_t(t) * nv + v) : make_float4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          a[0] += __float2ll_rn(f[u].x * 1073741824.0f);
+          a[1] += __float2ll_rn(f[u].y * 1073741824.0f);
+          a[2] += __float2ll_rn(f[u].z * 1073741824.0f);
+          a[3] += __float2ll_rn(f[u].w * 1073741824.0f);
+        }
       }
+    }
     // the count reduction above is done with the ring: reuse it
     long long *red = reinterpret_cast<long long *>(ring);  // [RG][psum_pitch]
     if (g < RG)
@@ -633,12 +690,14 @@ cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   p.nstages = nst;
   p.hist_pitch = (a.k * a.E + 3) & ~3;
   p.psum_pitch = (a.E + 3) & ~3;
-  // the ring also holds the epilogue's transpose tiles and phase B's
-  // reduction scratch
+  // the ring also holds the epilogue's shared tiles (8 warps, each with
+  // its half of the 32-expert chunks) and phase B's reduction scratch
+  p.chunks_per_warp = ((a.E + 31) / 32 + 1) / 2;
   size_t ring = size_t(nst) * p.stage_bytes;
   const int rg_aux = std::max(1, kGrThreads / (p.psum_pitch >> 2));
-  const size_t need = std::max({size_t(4) * kStgFloats * 4, size_t(2) * kGrThreads * 16,
-                                size_t(rg_aux) * p.psum_pitch * 8});
+  const size_t need =
+      std::max({size_t(8) * p.chunks_per_warp * kStgFloats * 4, size_t(2) * kGrThreads * 16,
+                size_t(rg_aux) * p.psum_pitch * 8});
   if (ring < need) return cudaErrorNotSupported;
   const size_t smem = fixed + ring;
   if (smem > kSmemLimit) return cudaErrorNotSupported;

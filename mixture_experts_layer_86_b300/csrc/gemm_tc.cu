@@ -599,7 +599,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     const int gw = warp - (2 + kPairEpiWarps);
     const int c16 = lane & 7, rsub = lane >> 3;
     const uint32_t full_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.full[0]), 0);
-    int stage = 0, pend = -1;
+    // stages whose copies are in flight, oldest first: up to the whole ring,
+    // as many as the TMA producer keeps in flight
+    int stage = 0, pend_head = 0, npend = 0;
+    int pend_q[kPairStages];
     uint32_t phase = 0;
     bool ok = true;
     for (int t = cid; t < total && ok; t += ncl) {
@@ -643,13 +646,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
           }
         }
         ptx::cp_async_commit();
-        if (pend >= 0) {  // the previous stage's copies have landed: hand it to the MMA
-          ptx::cp_async_wait<1>();
+        pend_q[(pend_head + npend) % kPairStages] = stage;
+        if (++npend == kPairStages) {
+          // the oldest stage's copies have landed: hand it to the MMA
+          ptx::cp_async_wait<kPairStages - 1>();
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend) * 8u);
+          if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend_q[pend_head]) * 8u);
+          pend_head = (pend_head + 1) % kPairStages;
+          --npend;
         }
-        pend = stage;
         if (++stage == kPairStages) {
           stage = 0;
           phase ^= 1u;
@@ -657,10 +663,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       }
     }
     ptx::cp_async_wait<0>();
-    if (pend >= 0) {
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend) * 8u);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    for (; npend > 0; --npend) {
+      if (lane == 0) ptx::mbar_arrive_remote(full_leader + uint32_t(pend_q[pend_head]) * 8u);
+      pend_head = (pend_head + 1) % kPairStages;
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
@@ -1029,15 +1036,24 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // 256 columns of B (tcgen05 splits B's N between the pair), 128 K rows per
 // stage: 64 KB per CTA per stage instead of the 96 KB that a single-CTA
 // 128 x 256 tile needs for the same work.
-//   both CTAs  warp 0: TMA loads of this CTA's halves into its ring, landing
-//              on its own `full` barrier; warp 10: waits `full`, zeroes the
-//              rows past the group (they may hold the next group's rows or
-//              unwritten memory), sums A's columns over the group's rows
-//              when the tile is the first N tile (the bias gradient
-//              db_g = sum over rows of A), and arrives on the even CTA's
-//              `ready` barrier; warps 2..9: epilogue of this CTA's 128 rows
-//   even CTA   warp 1: waits `ready` (both CTAs' arrivals), issues the pair
-//              MMAs; commits are multicast to both CTAs' `empty` / `tfull`.
+// A stage takes one of two paths:
+//   direct  (a K block wholly inside the group, no column sums): both CTAs'
+//           TMA copies complete on the even CTA's `full` barrier, which the
+//           MMA waits on -- the forward pair GEMM's path;
+//   relayed (the group's last, partial K block -- its rows past the group
+//           hold the next group's rows or unwritten memory and must read as
+//           zero -- or any K block of a first-N tile, whose A columns also
+//           give the bias gradient db_g = sum over rows of A): each CTA's
+//           copies complete on its own `tail` barrier; its warp 10 zeroes
+//           the rows past the group, adds A's columns, fences the stage for
+//           the tensor cores and arrives on the even CTA's `ready` barrier,
+//           which the MMA waits on.
+// Both CTAs walk the same tiles and K blocks, so every role agrees on each
+// stage's path; the phase of each barrier kind is tracked per stage.
+//   both CTAs  warp 0: TMA producer; warp 10: the relay; warps 2..9:
+//              epilogue of this CTA's 128 rows of the tile
+//   even CTA   warp 1: the pair MMAs; commits are multicast to both CTAs'
+//              `empty` / `tfull` barriers.
 constexpr int kWpBK = 128;                   // K rows per stage (two 64-row halves)
 constexpr int kWpStages = 3;
 constexpr uint32_t kWpBoxBytes = 64 * 64 * 2;               // 64 cols x 64 rows, 8 KB
@@ -1047,8 +1063,9 @@ constexpr int kWpFixupWarp = 2 + kWpEpiWarps;
 constexpr int kWpThreads = 32 * (kWpFixupWarp + 1);
 
 struct __align__(8) WpCtl {
-  uint64_t full[kWpStages];
-  uint64_t ready[kWpStages];
+  uint64_t full[kWpStages];    // even CTA: direct stages, both CTAs' bytes
+  uint64_t tail[kWpStages];    // each CTA: relayed stages, its own bytes
+  uint64_t ready[kWpStages];   // even CTA: relayed stages, both relays
   uint64_t empty[kWpStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -1057,6 +1074,11 @@ struct __align__(8) WpCtl {
   int abort;
 };
 constexpr size_t kWpSmemBytes = 1024 + kWpStages * 2 * kWpOpBytes + sizeof(WpCtl);
+
+// whether K block kb of a group with `rows` rows goes through the relay
+__device__ __forceinline__ bool wp_relayed(int rows, int kb, bool sum) {
+  return sum || rows - kb * kWpBK < kWpBK;
+}
 
 // Stage layout of one operand half: [k half 0: cols 0-63, cols 64-127]
 // [k half 1: cols 0-63, cols 64-127], each box 64 K rows of 128 B
@@ -1079,11 +1101,13 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const int mt = (M + 255) / 256, nt = (N + 255) / 256;
   const int total = G * mt * nt;
+  const bool with_sum = colsum != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWpStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 2);  // the fixup warp of each CTA
+      ptx::mbar_init(ptx::smem_addr(&ctl.tail[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 2);  // the relay of each CTA
       ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -1114,13 +1138,16 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_phase = 0;
+      uint32_t phase = 0;
+      uint32_t tail_armed = 0, tail_ph = 0;  // relayed fills not yet seen land here
       bool ok = true;
+      const uint32_t full_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.full[0]), 0);
       for (int t = cid; t < total && ok; t += ncl) {
         int g, m, n;
         wg_tile(t, mt, nt, g, m, n);
         const int r0 = offsets[g], rows = offsets[g + 1] - r0;
         const int nk = (rows + kWpBK - 1) / kWpBK;
+        const bool sum = with_sum && n == 0;
         const int acol = m * 256 + int(rank) * 128, bcol = n * 256 + int(rank) * 128;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort,
@@ -1130,41 +1157,63 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             ok = false;
             break;
           }
-          const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
-          ptx::mbar_arrive_expect_tx(fb, 2 * kWpOpBytes);
           const int row = r0 + kb * kWpBK;
+          if (wp_relayed(rows, kb, sum)) {
+            const uint32_t tb = ptx::smem_addr(&ctl.tail[stage]);
+            ptx::mbar_arrive_expect_tx(tb, 2 * kWpOpBytes);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
-              ptx::tma_load_2d(ptx::smem_addr(sA + off), &tmA, fb, acol + j * 64, row + h * 64);
-              ptx::tma_load_2d(ptx::smem_addr(sB + off), &tmB, fb, bcol + j * 64, row + h * 64);
-            }
-          armed |= 1u << stage;
-          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
+                ptx::tma_load_2d(ptx::smem_addr(sA + off), &tmA, tb, acol + j * 64, row + h * 64);
+                ptx::tma_load_2d(ptx::smem_addr(sB + off), &tmB, tb, bcol + j * 64, row + h * 64);
+              }
+            tail_armed |= 1u << stage;
+            tail_ph ^= 1u << stage;
+          } else {
+            const uint32_t fb = full_leader + uint32_t(stage) * 8u;
+            if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl.full[stage]),
+                                                      4 * kWpOpBytes);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
+                ptx::tma_load_2d_pair(ptx::smem_addr(sA + off), &tmA, fb, acol + j * 64,
+                                      row + h * 64);
+                ptx::tma_load_2d_pair(ptx::smem_addr(sB + off), &tmB, fb, bcol + j * 64,
+                                      row + h * 64);
+              }
+          }
           if (++stage == kWpStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // every stage filled here has been read by the pair's MMAs before the
-      // CTA moves on (or, after a give-up, at least its copies have landed)
-      for (int s = 0; s < kWpStages; ++s)
-        if (armed & (1u << s)) {
-          if (ok)
-            ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[s]), (armed_phase >> s) & 1u,
-                                   nullptr, kWaitLimitNs);
-          else
-            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+      if (!ok) {
+        // relayed copies issued here land before the CTA moves on
+        for (int s = 0; s < kWpStages; ++s)
+          if (tail_armed & (1u << s))
+            ptx::mbar_wait(ptx::smem_addr(&ctl.tail[s]), ((tail_ph >> s) & 1u) ^ 1u, nullptr,
                            kWaitLimitNs / 4);
+      }
+      // every stage filled here has been read by the pair's MMAs before the
+      // CTA moves on: the next fill of each stage would wait for exactly that
+      for (int i = 0; i < kWpStages && ok; ++i) {
+        ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, nullptr,
+                               kWaitLimitNs);
+        if (++stage == kWpStages) {
+          stage = 0;
+          phase ^= 1u;
         }
+      }
     }
   } else if (warp == kWpFixupWarp) {
-    // ------------ fixup: rows past the group, bias-gradient column sums
+    // ------------------------------ the relay of relayed stages (see above)
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t tail_ph = 0;
     bool ok = true;
     const uint32_t ready_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.ready[0]), 0);
     // this lane's 4 columns of A (of the CTA's 128): box j, 16-byte chunk, offset
@@ -1174,12 +1223,17 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       wg_tile(t, mt, nt, g, m, n);
       const int rows = offsets[g + 1] - offsets[g];
       const int nk = (rows + kWpBK - 1) / kWpBK;
-      const bool sum = colsum != nullptr && n == 0;
+      const bool sum = with_sum && n == 0;
       float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       for (int kb = 0; kb < nk; ++kb) {
+        const int st = stage;
+        if (++stage == kWpStages) stage = 0;
+        if (!wp_relayed(rows, kb, sum)) continue;
         bool got = true;
         if (lane == 0)
-          got = ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs);
+          got = ptx::mbar_wait(ptx::smem_addr(&ctl.tail[st]), (tail_ph >> st) & 1u, abort,
+                               kWaitLimitNs);
+        tail_ph ^= 1u << st;
         got = __shfl_sync(kFullMask, got ? 1 : 0, 0) != 0;
         if (!got) {
           if (lane == 0) {
@@ -1198,21 +1252,20 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             const int nbytes = (64 - vr) * 128;              // contiguous tail of each box
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-              const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes + vr * 128;
+              const uint32_t off = st * kWpOpBytes + (h * 2 + j) * kWpBoxBytes + vr * 128;
               for (int i = lane * 16; i < nbytes; i += 32 * 16) {
                 *reinterpret_cast<uint4 *>(sA + off + i) = z;
                 *reinterpret_cast<uint4 *>(sB + off + i) = z;
               }
             }
           }
-          ptx::fence_proxy_async_smem();
         }
         __syncwarp();
         if (sum) {
           // rows past the group are zero now: add all 128 rows, in order
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint8_t *box = sA + stage * kWpOpBytes + (h * 2 + cj) * kWpBoxBytes;
+            const uint8_t *box = sA + st * kWpOpBytes + (h * 2 + cj) * kWpBoxBytes;
 #pragma unroll 4
             for (int kr = 0; kr < 64; ++kr) {
               const uint2 v = *reinterpret_cast<const uint2 *>(
@@ -1223,15 +1276,10 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
               acc[3] += __uint_as_float(v.y & 0xffff0000u);
             }
           }
-          __syncwarp();
         }
         ptx::fence_proxy_async_smem();  // this CTA's stage is complete for the MMA's reads
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_remote(ready_leader + uint32_t(stage) * 8u);
-        if (++stage == kWpStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (lane == 0) ptx::mbar_arrive_remote(ready_leader + uint32_t(st) * 8u);
       }
       if (sum && ok) {
         const int col = m * 256 + int(rank) * 128 + cj * 64 + cchunk * 8 + (csub >> 1);
@@ -1247,13 +1295,14 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint64_t a_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sA), kWpBoxBytes, 1024);
       const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), kWpBoxBytes, 1024);
       int stage = 0, it = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, full_ph = 0, ready_ph = 0;
       bool ok = true;
       for (int t = cid; t < total && ok; t += ncl, ++it) {
         int g, m, n;
         wg_tile(t, mt, nt, g, m, n);
         const int rows = offsets[g + 1] - offsets[g];
         const int nk = (rows + kWpBK - 1) / kWpBK;
+        const bool sum = with_sum && n == 0;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort,
@@ -1265,8 +1314,15 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * 256);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.ready[stage]), phase, abort,
-                                      kWaitLimitNs)) {
+          const bool relayed = wp_relayed(rows, kb, sum);
+          const uint32_t bar =
+              ptx::smem_addr(relayed ? &ctl.ready[stage] : &ctl.full[stage]);
+          const uint32_t par = ((relayed ? ready_ph : full_ph) >> stage) & 1u;
+          if (relayed)
+            ready_ph ^= 1u << stage;
+          else
+            full_ph ^= 1u << stage;
+          if (!ptx::mbar_wait_cluster(bar, par, abort, kWaitLimitNs)) {
             record_error(err, kErrWgradMma | uint32_t(t & 0x7fffff));
             *abort = 1;
             ok = false;
@@ -1291,6 +1347,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       ptx::mma_commit_pair(ptx::smem_addr(&ctl.drain));
       if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
         record_error(err, kErrGemmDrain);
+      (void)phase;
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
