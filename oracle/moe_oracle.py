@@ -365,9 +365,15 @@ class LayerConfig:
     dtype: str = "bf16"             # the router input's storage under jitter: bf16 | f32 | f64
 
 
+def uses_selection_noise(cfg: LayerConfig) -> bool:
+    """Whether the expert choice reads Gumbel keys (R11 rsample, R13
+    second-expert sampling with k = 2)."""
+    return cfg.noise_policy == "rsample" or (cfg.second_expert_sampling and cfg.k == 2)
+
+
 def selection_noise(cfg: LayerConfig, num_tokens: int) -> Optional[np.ndarray]:
     """The Gumbel noise g[s,e] the choice uses (R11, R13), or None."""
-    if cfg.noise_policy == "rsample" or (cfg.second_expert_sampling and cfg.k == 2):
+    if uses_selection_noise(cfg):
         return RS.gate_noise(num_tokens, cfg.num_experts, cfg.noise_seed, cfg.noise_offset)[1]
     return None
 
@@ -377,13 +383,14 @@ def select_experts(logits: np.ndarray, cfg: LayerConfig, noise=None) -> np.ndarr
     top-k of the logits; top-k of the float32 keys logits + g (rsample,
     R11); or the noise-free first choice and the second from the keys
     (second-expert sampling, R13).  ``noise``: g (float, [S,E]); drawn from
-    the layer's stream when None."""
+    the layer's stream when None; ignored when neither option is on (jitter
+    and random token selection leave the choice on the logits)."""
     lg = np.asarray(logits, np.float64)
     S = lg.shape[0]
+    if not uses_selection_noise(cfg):
+        return topk_experts(lg, cfg.k)
     if noise is None:
         noise = selection_noise(cfg, S)
-    if noise is None:
-        return topk_experts(lg, cfg.k)
     keys = (lg.astype(np.float32) + np.asarray(noise).astype(np.float32)).astype(np.float64)
     if cfg.noise_policy == "rsample":
         return topk_experts(keys, cfg.k)

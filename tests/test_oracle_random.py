@@ -155,6 +155,21 @@ def test_rsample_keys_are_float32_sums():
     assert O.topk_experts(lg, 1)[0, 0] == 1               # not in float64
 
 
+@pytest.mark.parametrize("opts", [dict(), dict(noise_policy="jitter"), dict(use_rts=True),
+                                  dict(second_expert_sampling=True)])
+def test_noise_leaves_the_choice_alone_unless_an_option_reads_it(opts):
+    """Only rsample and second-expert sampling with k = 2 choose on Gumbel
+    keys; jitter, random token selection and k = 1 choose on the logits
+    whatever noise is passed."""
+    k = 1 if opts.get("second_expert_sampling") else 2
+    c = O.LayerConfig(64, 8, 8, 4, k, 1.0, 1, True, "relu", **opts)
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((64, 4))
+    g = 50.0 * rng.standard_normal((64, 4))               # would reorder almost every row
+    assert np.array_equal(O.select_experts(lg, c, g), O.topk_experts(lg, k))
+    assert np.array_equal(O.route(lg, c, noise=g)["routing"].idx, O.topk_experts(lg, k))
+
+
 # --------------------------------------------------------------------------
 # random token selection
 # --------------------------------------------------------------------------
