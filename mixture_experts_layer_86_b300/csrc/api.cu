@@ -114,21 +114,31 @@ struct BwdWs {
   void *d_out, *dh_pre, *dx_disp;
   float *dw, *dlogits, *gate_partial;
   float *aux_coef;
-  void *xj;  // the jittered router input (MOE_NOISE_JITTER only)
+  void *xj;       // the jittered router input (MOE_NOISE_JITTER only)
+  int32_t *rows;  // [S, k] row of each choice in the expert-major buffers, -1 when dropped
 };
 
+// The router's backward: fp32 layers keep dlogits [S,E] fp32 and CUDA-core
+// partials; bf16 layers keep the [S, 2P] hi/lo operand (in the dlogits
+// slot) and the tensor-core chunk partials.
 size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const int64_t R = max_rows_of(c);
   const size_t eb = elem_bytes(c->dtype);
-  const size_t sz[8] = {align256(size_t(R) * c->hidden_size * eb),
+  const int64_t S = c->num_tokens;
+  const bool tc = c->dtype == MOE_BF16;
+  const size_t sz[9] = {align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
-                        align256(size_t(c->num_tokens) * c->k * 4),
-                        align256(size_t(c->num_tokens) * c->num_experts * 4),
-                        align256(gate_wgrad_partial_bytes(c->num_tokens, c->num_experts,
-                                                          c->hidden_size)),
+                        align256(size_t(S) * c->k * 4),
+                        align256(tc ? size_t(S) * 2 * router_pad(c->num_experts) * 2
+                                    : size_t(S) * c->num_experts * 4),
+                        align256(tc ? gate_wgrad_tc_partial_bytes(S, c->num_experts,
+                                                                  c->hidden_size)
+                                    : gate_wgrad_partial_bytes(S, c->num_experts,
+                                                               c->hidden_size)),
                         align256(size_t(c->num_experts) * 4),
-                        jitter_bytes(c)};
+                        jitter_bytes(c),
+                        align256(size_t(S) * c->k * 4)};
   if (w) {
     char *p = static_cast<char *>(base);
     w->d_out = p; p += sz[0];
@@ -138,7 +148,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->dlogits = reinterpret_cast<float *>(p); p += sz[4];
     w->gate_partial = reinterpret_cast<float *>(p); p += sz[5];
     w->aux_coef = reinterpret_cast<float *>(p); p += sz[6];
-    w->xj = sz[7] ? p : nullptr;
+    w->xj = sz[7] ? p : nullptr; p += sz[7];
+    w->rows = reinterpret_cast<int32_t *>(p);
   }
   size_t total = 0;
   for (size_t v : sz) total += v;
@@ -567,7 +578,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
 
   // 1. dO = w * dY per kept row; dw = <dY, out>
   MOE_CUDA(launch_combine_bwd(dy, sv->out_disp, dt, S, d, k, sv->topk_idx, sv->slot,
-                              sv->expert_offsets, sv->topk_w, w.d_out, w.dw, st));
+                              sv->expert_offsets, sv->topk_w, w.d_out, w.dw, st, w.rows));
   // 2. dW2_e = dO_e^T h_e ; db2 = column sums of dO (in the same kernel
   //    when the CTA-pair weight-gradient GEMM runs)
   bool db2_done = false;
@@ -660,19 +671,30 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
   // 6. router: dlogits, dW_g = dlogits^T x (the router saw x * f under jitter)
   MOE_CUDA(launch_aux_coef(sv->topk_idx, sv->probs, S, k, E, cfg->aux_loss_type, w.aux_coef,
                            st));
+  const bool tc = dt == MOE_BF16;
+  void *dl2 = tc ? static_cast<void *>(w.dlogits) : nullptr;
   MOE_CUDA(launch_gate_bwd(sv->probs, sv->topk_idx, w.dw, w.aux_coef, S, E, k,
-                           cfg->aux_loss_weight, inv_temperature(cfg), w.dlogits, st));
+                           cfg->aux_loss_weight, inv_temperature(cfg), tc ? nullptr : w.dlogits,
+                           dl2, router_pad(E), st));
   const RouteNoise noise = noise_of(cfg);
+  const RouteNoise *jit = noise.policy == MOE_NOISE_JITTER ? &noise : nullptr;
   const void *xr = x;
-  if (noise.policy == MOE_NOISE_JITTER) {
+  if (jit) {
     MOE_CUDA(launch_jitter(x, dt, S, d, noise, w.xj, st));
     xr = w.xj;
+  }
+  if (tc) {
+    // on the tensor cores: dW_g from x^T [hi | lo]; dX from [hi | lo] [W_g; W_g]
+    // with the experts' rows added in the GEMM's epilogue
+    MOE_CUDA(launch_gate_wgrad_tc(xr, dl2, S, d, E, w.gate_partial, dw_gate,
+                                  device_error_ptr(), st));
+    return cuda_status(launch_dx_router_tc(dl2, w_gate, w.dx_disp, S, d, E, k, w.rows, dx, jit,
+                                           device_error_ptr(), st));
   }
   MOE_CUDA(launch_gate_wgrad(w.dlogits, xr, dt, S, d, E, w.gate_partial, dw_gate, st));
   // 7. dX = sum_j dx_disp[row] + (dlogits W_g) (* f under jitter)
   return cuda_status(launch_dx_combine(w.dx_disp, w.dlogits, w_gate, dt, S, d, E, k,
-                                       sv->topk_idx, sv->slot, sv->expert_offsets, dx, st,
-                                       noise.policy == MOE_NOISE_JITTER ? &noise : nullptr));
+                                       sv->topk_idx, sv->slot, sv->expert_offsets, dx, st, jit));
 }
 
 moe_status moe_debug_set_wait_limit(uint64_t ns) {

@@ -194,7 +194,89 @@ dx_combine_tile_kernel(const T *__restrict__ dx_disp, const float *__restrict__ 
   }
 }
 
+// ------------------------------------------- dW_g from tensor-core partials
+// dW_g[e, c] = sum over chunks g of (part[g, c, e] + part[g, c, P + e]): the
+// hi and lo halves of each chunk's x^T [hi | lo], added in chunk order.
+// CTA: 8 columns c (one per warp) x 32 experts e (one per lane), every
+// chunk's loads in flight together; written along c through shared memory.
+__global__ void __launch_bounds__(256)
+gate_wgrad_tc_reduce_kernel(const float *__restrict__ part, int nchunk, int d, int E, int P,
+                            int dtype, void *__restrict__ dw_gate) {
+  griddep_begin();
+  __shared__ float tile[32][9];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 8 + w, e = blockIdx.y * 32 + lane;
+  float acc = 0.0f;
+  if (c < d && e < E) {
+    const float *p = part + int64_t(c) * (2 * P) + e;
+    const int64_t step = int64_t(d) * (2 * P);
+#pragma unroll 8
+    for (int g = 0; g < nchunk; ++g) acc += __ldcs(p + g * step) + __ldcs(p + g * step + P);
+  }
+  tile[lane][w] = acc;
+  __syncthreads();
+  // thread t writes expert e0 + t / 8, column c0 + t % 8
+  const int eo = blockIdx.y * 32 + (threadIdx.x >> 3), co = blockIdx.x * 8 + (threadIdx.x & 7);
+  if (eo < E && co < d)
+    store_elem(dw_gate, dtype, int64_t(eo) * d + co, tile[threadIdx.x >> 3][threadIdx.x & 7]);
+}
+
 }  // namespace
+
+// token chunks of the dW_g product: as many (chunk, 128-column) tiles as
+// fit in one wave over the SMs, chunks a multiple of the 64-row K block
+static int gate_wgrad_tc_chunk_rows(int64_t S, int d) {
+  const int ctiles = (d + 127) / 128;
+  int64_t want = num_sms() / ctiles;
+  if (want < 1) want = 1;
+  const int64_t per = (S + want - 1) / want;
+  return int(per < 64 ? 64 : (per + 63) / 64 * 64);
+}
+
+int gate_wgrad_tc_chunks(int64_t S, int d) {
+  const int64_t rows = gate_wgrad_tc_chunk_rows(S, d);
+  const int64_t n = (S + rows - 1) / rows;
+  return int(n < 1 ? 1 : n);
+}
+
+size_t gate_wgrad_tc_partial_bytes(int64_t S, int E, int d) {
+  return size_t(gate_wgrad_tc_chunks(S, d)) * d * 2 * router_pad(E) * 4;
+}
+
+cudaError_t launch_gate_wgrad_tc(const void *x, const void *dl2, int64_t S, int d, int E,
+                                 float *partial, void *dw_gate, unsigned int *err,
+                                 cudaStream_t st) {
+  const int P = router_pad(E);
+  const dim3 grid(unsigned((d + 7) / 8), unsigned((E + 31) / 32));
+  if (S <= 0)  // no tokens: dW_g = 0
+    return launch_k(gate_wgrad_tc_reduce_kernel, grid, 256, 0, st,
+                    static_cast<const float *>(partial), 0, d, E, P, int(MOE_BF16), dw_gate);
+  const int nch = gate_wgrad_tc_chunks(S, d);
+  TcWgrad g{};
+  g.A = x; g.B = dl2; g.rows_alloc = S;
+  g.M = d; g.N = 2 * P; g.G = nch;
+  g.offsets = nullptr; g.chunk_rows = gate_wgrad_tc_chunk_rows(S, d);
+  g.Cf = partial; g.single = true; g.err = err;
+  if (const cudaError_t e = launch_tc_wgrad(g, st); e != cudaSuccess) return e;
+  return launch_k(gate_wgrad_tc_reduce_kernel, grid, 256, 0, st,
+                  static_cast<const float *>(partial), nch, d, E, P, int(MOE_BF16), dw_gate);
+}
+
+cudaError_t launch_dx_router_tc(const void *dl2, const void *w_gate, const void *dx_disp,
+                                int64_t S, int d, int E, int k, const int32_t *rows, void *dx,
+                                const RouteNoise *jitter, unsigned int *err, cudaStream_t st) {
+  if (S <= 0) return cudaSuccess;
+  const int P = router_pad(E);
+  TcGemm g{};
+  g.A = dl2; g.rows_alloc = S; g.B = w_gate; g.b_kmajor = false; g.C = dx;
+  g.N = d; g.K = 2 * P; g.G = 1; g.offsets = nullptr; g.bias = nullptr; g.act = -1;
+  g.pre = nullptr; g.grad_src = nullptr; g.dact = 0; g.err = err;
+  g.b_wrap = P; g.b_rows = E;
+  g.rt.src = dx_disp; g.rt.rows = rows; g.rt.k = k;
+  g.rt.jitter = jitter ? 1 : 0;
+  if (jitter) g.rt.noise = *jitter;
+  return launch_tc_gemm(g, st);
+}
 
 int64_t gate_wgrad_splits(int64_t S) {
   int64_t n = (S + 255) / 256;

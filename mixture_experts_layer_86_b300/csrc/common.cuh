@@ -56,6 +56,30 @@ __device__ __forceinline__ float act_grad(float z, int act) {
   return 0.5f * (1.0f + erff(z * 0.7071067811865476f)) + z * pdf;
 }
 
+// ---- l_aux statistics without FP64 arithmetic (the FP64 rate of this GPU
+// is a small fraction of its FP32 rate, and these run on a single warp).
+// Inputs: per-expert probability sums A_e in units of 2^-30 (exact integer
+// sums, so the order of addition does not matter) and first-choice counts.
+constexpr float kFix30 = 1073741824.0f;        // 2^30
+constexpr float kInvFix30 = 9.313225746154785e-10f;  // 2^-30
+
+// signed 128-bit integer to the nearest-ish float (two roundings)
+__device__ __forceinline__ float i128_to_float(__int128 v) {
+  const bool neg = v < 0;
+  const unsigned __int128 m = neg ? (unsigned __int128)(-v) : (unsigned __int128)v;
+  const float f = __ull2float_rn((unsigned long long)(m >> 64)) * 18446744073709551616.0f +
+                  __ull2float_rn((unsigned long long)m);
+  return neg ? -f : f;
+}
+
+// (u_e - mean_e u) for the usage u_e = A_e 2^-30 / S: the deviation is
+// formed exactly as A_e E - sum A in 128-bit integers, then scaled once.
+__device__ __forceinline__ float usage_deviation(long long A_e, long long sum_A, int E,
+                                                 int64_t S) {
+  const __int128 dev = (__int128)A_e * E - (__int128)sum_A;  // (u_e - mean) S E 2^30
+  return i128_to_float(dev) * kInvFix30 / (float(S) * float(E));
+}
+
 // 16-byte vector of row elements and its conversion to / from fp32.
 template <typename T> struct Vec;
 template <> struct Vec<float> {

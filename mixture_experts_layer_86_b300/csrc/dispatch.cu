@@ -136,7 +136,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
                    int64_t S, int nvec, int k, const int32_t *__restrict__ idx,
                    const int32_t *__restrict__ slot, const int32_t *__restrict__ offsets,
                    const float *__restrict__ w, uint4 *__restrict__ d_out,
-                   float *__restrict__ dw) {
+                   float *__restrict__ dw, int32_t *__restrict__ rows) {
   griddep_begin();
   using V = Vec<T>;
   const int lane = threadIdx.x & 31;
@@ -144,6 +144,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
   if (s >= S) return;
   for (int j = 0; j < k; ++j) {
     const int64_t r = row_of(idx, slot, offsets, s * k + j);
+    if (rows && lane == 0) rows[s * k + j] = int32_t(r);
     if (r < 0) {
       if (lane == 0) dw[s * k + j] = 0.0f;
       continue;
@@ -194,28 +195,30 @@ __global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N
 __global__ void aux_coef_kernel(const int32_t *__restrict__ idx, const float *__restrict__ probs,
                                 int64_t S, int k, int E, int aux_type, float *__restrict__ coef) {
   griddep_begin();
-  __shared__ double s_col[kMaxExperts];
-  __shared__ double s_part[1024];
+  // column sums of p in units of 2^-30: exact integer sums (no FP64; the
+  // order of addition does not matter)
+  __shared__ long long s_col[kMaxExperts];
+  __shared__ long long s_part[1024];
   __shared__ int32_t cnt[kMaxExperts];
-  __shared__ double s_stat[2];
+  __shared__ float s_std;
+  __shared__ long long s_sum;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     cnt[e] = 0;
-    s_col[e] = 0.0;
+    s_col[e] = 0;
   }
   __syncthreads();
   if (aux_type == MOE_AUX_STD) {
-    // column sums of p: G token groups per column (consecutive threads on
-    // consecutive columns), then the groups added in a fixed order
+    // G token groups per column (consecutive threads on consecutive columns)
     const int G = int(blockDim.x) / E;
     const int e = threadIdx.x % E, grp = threadIdx.x / E;
     if (grp < G) {
-      double acc = 0.0;
-      for (int64_t s = grp; s < S; s += G) acc += double(probs[s * E + e]);
+      long long acc = 0;
+      for (int64_t s = grp; s < S; s += G) acc += __float2ll_rn(probs[s * E + e] * kFix30);
       s_part[grp * E + e] = acc;
     }
     __syncthreads();
     for (int c = threadIdx.x; c < E; c += blockDim.x) {
-      double acc = 0.0;
+      long long acc = 0;
       for (int g = 0; g < G; ++g) acc += s_part[g * E + c];
       s_col[c] = acc;
     }
@@ -223,27 +226,36 @@ __global__ void aux_coef_kernel(const int32_t *__restrict__ idx, const float *__
     for (int64_t s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&cnt[idx[s * k]], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0 && aux_type == MOE_AUX_STD) {
-    double su = 0.0, sq = 0.0;
-    for (int e = 0; e < E; ++e) su += s_col[e] / double(S);
-    const double mean = su / double(E);
-    for (int e = 0; e < E; ++e) {
-      const double dv = s_col[e] / double(S) - mean;
-      sq += dv * dv;
+  if (threadIdx.x < 32 && aux_type == MOE_AUX_STD) {
+    // population std of u_e = sum_s p[s,e] / S over the experts
+    const int lane = threadIdx.x;
+    long long sa = 0;
+    for (int e = lane; e < E; e += 32) sa += s_col[e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(kFullMask, sa, o);
+    float sq = 0.0f;
+    if (S > 0)
+      for (int e = lane; e < E; e += 32) {
+        const float dv = usage_deviation(s_col[e], sa, E, S);
+        sq = fmaf(dv, dv, sq);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
+    if (lane == 0) {
+      s_std = sqrtf(sq / float(E));
+      s_sum = sa;
     }
-    s_stat[0] = mean;
-    s_stat[1] = sqrt(sq / double(E));
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double c;
+    float c;
     if (aux_type == MOE_AUX_STD)
-      c = s_stat[1] > 0.0 ? (s_col[e] / double(S) - s_stat[0]) /
-                                (double(E) * double(S) * s_stat[1])
-                          : 0.0;
+      c = s_std > 0.0f ? usage_deviation(s_col[e], s_sum, E, S) /
+                             (float(E) * float(S) * s_std)
+                       : 0.0f;
     else
-      c = double(E) * double(cnt[e]) / (double(S) * double(S));
-    coef[e] = float(c);
+      c = float(E) * float(cnt[e]) / float(S) / float(S);
+    coef[e] = c;
   }
 }
 
@@ -252,7 +264,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx,
                 const float *__restrict__ dw, const float *__restrict__ coef,
                 int64_t S, int E, int k, float aux_w, float inv_temp,
-                float *__restrict__ dlogits) {
+                float *__restrict__ dlogits, __nv_bfloat16 *__restrict__ dl2, int P) {
   griddep_begin();
   const int lane = threadIdx.x & 31;
   const int64_t s = int64_t(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
@@ -284,8 +296,19 @@ gate_bwd_kernel(const float *__restrict__ probs, const int32_t *__restrict__ idx
     float dp = aux_w * coef[e];
     if (e == i1) dp += g1;
     if (e == i2) dp += g2;
-    dlogits[s * E + e] = inv_temp * p[e] * (dp - dot);  // the softmax saw logits / T
+    const float dl = inv_temp * p[e] * (dp - dot);  // the softmax saw logits / T
+    if (dlogits) dlogits[s * E + e] = dl;
+    if (dl2) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(dl);
+      dl2[s * 2 * P + e] = hi;
+      dl2[s * 2 * P + P + e] = __float2bfloat16_rn(dl - __bfloat162float(hi));
+    }
   }
+  if (dl2)  // the padding columns of both halves
+    for (int e = E + lane; e < P; e += 32) {
+      dl2[s * 2 * P + e] = __float2bfloat16_rn(0.0f);
+      dl2[s * 2 * P + P + e] = __float2bfloat16_rn(0.0f);
+    }
 }
 
 inline unsigned token_blocks(int64_t S) { return unsigned((S + kWarpsPerCta - 1) / kWarpsPerCta); }
@@ -335,7 +358,7 @@ cudaError_t launch_residual_mix(const void *x, int dtype, int64_t S, int d, cons
 cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, int64_t S,
                                int d, int k, const int32_t *idx, const int32_t *slot,
                                const int32_t *offsets, const float *w, void *d_out, float *dw,
-                               cudaStream_t st) {
+                               cudaStream_t st, int32_t *rows) {
   if (S == 0) return cudaSuccess;
   const int nvec = d * elem_bytes(dtype) / 16;
   auto *dy4 = static_cast<const uint4 *>(dy);
@@ -343,9 +366,9 @@ cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, 
   auto *do4 = static_cast<uint4 *>(d_out);
   if (dtype == MOE_F32)
     return launch_k(combine_bwd_kernel<float>, token_blocks(S), kWarpsPerCta * 32, 0, st, dy4, o4, S,
-                    nvec, k, idx, slot, offsets, w, do4, dw);
+                    nvec, k, idx, slot, offsets, w, do4, dw, rows);
   return launch_k(combine_bwd_kernel<__nv_bfloat16>, token_blocks(S), kWarpsPerCta * 32, 0, st, dy4,
-                  o4, S, nvec, k, idx, slot, offsets, w, do4, dw);
+                  o4, S, nvec, k, idx, slot, offsets, w, do4, dw, rows);
 }
 
 cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
@@ -362,10 +385,12 @@ cudaError_t launch_aux_coef(const int32_t *idx, const float *probs, int64_t S, i
 
 cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx, const float *dw,
                             const float *coef, int64_t S, int E, int k, float aux_w,
-                            float inv_temp, float *dlogits, cudaStream_t st) {
+                            float inv_temp, float *dlogits, void *dl2, int P,
+                            cudaStream_t st) {
   if (S == 0) return cudaSuccess;
   return launch_k(gate_bwd_kernel, token_blocks(S), kWarpsPerCta * 32, 0, st, probs, idx, dw,
-                  coef, S, E, k, aux_w, inv_temp, dlogits);
+                  coef, S, E, k, aux_w, inv_temp, dlogits,
+                  static_cast<__nv_bfloat16 *>(dl2), P);
 }
 
 }  // namespace moe

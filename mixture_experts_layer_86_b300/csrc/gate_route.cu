@@ -89,7 +89,6 @@ struct __align__(16) GrCtl {
   int barrier_ok;
   float bias[kMaxExperts];          // the [E] logit bias (zero without one)
   float psum_w[4][kMaxExperts];     // per-warp probability sums of the tile
-  int32_t wcnt[4][kMaxExperts];     // per-warp counts, then warp prefixes
   int32_t cnt[2][kMaxExperts];      // this tile's count per (j, e)
   int32_t pre[2][kMaxExperts];      // counts of the tiles before this one
   int32_t tot[2][kMaxExperts];      // counts of all tiles
@@ -164,6 +163,24 @@ __device__ __forceinline__ int comp4(const int4 &v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
+// the copies of ring stage kb % nstages: nbox K boxes of the tile's x rows
+// and of W_g, completing on the stage's `full` barrier
+__device__ __forceinline__ void issue_stage(const GrParams &p, const CUtensorMap *tmX,
+                                            const CUtensorMap *tmW, uint8_t *ring, GrCtl &ctl,
+                                            int kb, int64_t tok0) {
+  const int stage = kb % p.nstages;
+  const uint32_t wbox_bytes = uint32_t(p.E_pad) * 128;
+  const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
+  const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
+  uint8_t *st = ring + stage * p.stage_bytes;
+  ptx::mbar_arrive_expect_tx(fb, uint32_t(nb) * (uint32_t(p.TM) * 128 + wbox_bytes));
+  for (int b = 0; b < nb; ++b) {
+    const int k0 = (kb * p.nbox + b) * 64;
+    ptx::tma_load_2d(ptx::smem_addr(st + b * kXBoxBytes), tmX, fb, k0, int32_t(tok0));
+    ptx::tma_load_2d(ptx::smem_addr(st + p.nbox * kXBoxBytes + b * wbox_bytes), tmW, fb, k0, 0);
+  }
+}
+
 __global__ void __launch_bounds__(kGrThreads, 1)
 gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ GrParams p) {
@@ -189,10 +206,10 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     ptx::mbar_init(ptx::smem_addr(&ctl.done), 1);
     ctl.abort = 0;
     ptx::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tmX);
-    ptx::tma_prefetch_desc(&tmW);
+    // the first pass over the ring needs no empty slot: its copies start
+    // now, while the other warps set up (they write only the bytes past the
+    // TM rows of each x box, which the copies never touch)
+    for (int kb = 0; kb < p.nstages; ++kb) issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), p.tmem_cols);
@@ -223,9 +240,10 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   // ------------------------------------------------------------ phase A
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t armed = 0, armed_phase = 0;
+      // stages 0 .. nstages-1 were issued during the setup (phase 0)
+      uint32_t armed = (1u << p.nstages) - 1u, armed_phase = 0;
       bool ok = true;
-      for (int kb = 0; kb < p.nk; ++kb) {
+      for (int kb = p.nstages; kb < p.nk; ++kb) {
         const int stage = kb % p.nstages;
         const uint32_t phase = (kb / p.nstages) & 1;
         if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, lim)) {
@@ -234,16 +252,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
           ok = false;
           break;
         }
-        const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
-        const uint32_t fb = ptx::smem_addr(&ctl.full[stage]);
-        uint8_t *st = ring + stage * p.stage_bytes;
-        ptx::mbar_arrive_expect_tx(fb, uint32_t(nb) * (uint32_t(p.TM) * 128 + wbox_bytes));
-        for (int b = 0; b < nb; ++b) {
-          const int k0 = (kb * p.nbox + b) * 64;
-          ptx::tma_load_2d(ptx::smem_addr(st + b * kXBoxBytes), &tmX, fb, k0, int32_t(tok0));
-          ptx::tma_load_2d(ptx::smem_addr(st + p.nbox * kXBoxBytes + b * wbox_bytes), &tmW, fb,
-                           k0, 0);
-        }
+        issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
       }
@@ -406,9 +415,13 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         if (c * 32 + t < E) stg[lane * 33 + t] = valid ? stg[lane * 33 + t] * inv_z : 0.0f;
       __syncwarp();
       const int e = c * 32 + lane;
-      float cs = 0.0f;
-      for (int rr = 0; rr < 32; ++rr) cs += stg[rr * 33 + lane];
-      if (e < E) ctl.psum_w[q][e] = cs;
+      float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows rr = 4 i + u, fixed order
+#pragma unroll
+      for (int rr = 0; rr < 32; rr += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cs[u] += stg[(rr + u) * 33 + lane];
+      }
+      if (e < E) ctl.psum_w[q][e] = (cs[0] + cs[1]) + (cs[2] + cs[3]);
       if (p.probs)
         for (int rr = 0; rr < wrows; ++rr)
           if (e < E) p.probs[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
@@ -434,31 +447,38 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   block_sync();
 
   if (warp >= 4) {
-    // the tile's count and each token's rank per (j, e), in token order
+    // the tile's count and each token's rank per (j, e), in token order:
+    // within a warp by __match_any_sync, across the 4 warps by their counts'
+    // prefix; both choices at once, the counts in the ring (idle now)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int et = tid - 128;  // 0..127 over warps 4..7
-    for (int j = 0; j < k; ++j) {
-      for (int i = et; i < 4 * kMaxExperts; i += 128) (&ctl.wcnt[0][0])[i] = 0;
-      epi_sync();
-      const int e = ctl.choice[j][r];
-      const unsigned peers = __match_any_sync(kFullMask, e);
-      const int rk = __popc(peers & lanemask_lt());
-      if (e >= 0 && rk == 0) ctl.wcnt[q][e] = __popc(peers);
-      epi_sync();
-      for (int ee = et; ee < E; ee += 128) {
-        int run = 0;
-        for (int w4 = 0; w4 < 4; ++w4) {
-          const int cnum = ctl.wcnt[w4][ee];
-          ctl.wcnt[w4][ee] = run;
-          run += cnum;
-        }
-        ctl.cnt[j][ee] = run;
-      }
-      epi_sync();
-      ctl.rank[j][r] = e >= 0 ? ctl.wcnt[q][e] + rk : 0;
-      epi_sync();
+    int32_t *wc = reinterpret_cast<int32_t *>(ring);  // [k][4][E]
+    for (int i = et; i < k * 4 * E; i += 128) wc[i] = 0;
+    epi_sync();
+    int ej[2], rk[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      ej[j] = j < k ? ctl.choice[j][r] : -1;
+      const unsigned peers = __match_any_sync(kFullMask, ej[j]);
+      rk[j] = __popc(peers & lanemask_lt());
+      if (ej[j] >= 0 && rk[j] == 0) wc[(j * 4 + q) * E + ej[j]] = __popc(peers);
     }
+    epi_sync();
+    for (int i = et; i < k * E; i += 128) {
+      const int j = i / E, ee = i - j * E;
+      int run = 0;
+      for (int w4 = 0; w4 < 4; ++w4) {
+        const int cnum = wc[(j * 4 + w4) * E + ee];
+        wc[(j * 4 + w4) * E + ee] = run;
+        run += cnum;
+      }
+      ctl.cnt[j][ee] = run;
+    }
+    epi_sync();
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (j < k) ctl.rank[j][r] = ej[j] >= 0 ? wc[(j * 4 + q) * E + ej[j]] + rk[j] : 0;
   } else {
     // publish the tile's probability sums (padding entries 0)
     for (int e = tid; e < p.psum_pitch; e += 128)
@@ -498,9 +518,9 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
     const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
     if (g < RG && okb) {
-      // 16 rows per round, every load issued before any is used: the prefix
-      // costs a round trip to L2 per 16 * RG tiles
-      constexpr int kU = 16;
+      // 24 rows per round, every load issued before any is used: the prefix
+      // costs a round trip to L2 per 24 * RG tiles
+      constexpr int kU = 24;
       for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
         int4 a[kU];
 #pragma unroll
@@ -620,31 +640,33 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     }
     block_sync();
     if (warp == 0) {
+      // fp32 from the exact integer sums (no FP64): lane l owns a
+      // contiguous range of experts, lanes are added in a fixed tree order
       const int per = (E + 31) / 32;
       const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-      const double S = double(p.S);
-      double aux = 0.0;
-      for (int e = e0; e < e1; ++e)
-        aux += double(ctl.aux[e]) * (1.0 / 1073741824.0) * double(ctl.tot[0][e]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
+      const float S = float(p.S);
       if (p.aux_type == MOE_AUX_STD) {
         // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
-        double su = 0.0, sq = 0.0;
-        for (int e = e0; e < e1; ++e) su += double(ctl.aux[e]) * (1.0 / 1073741824.0) / S;
+        long long sa = 0;
+        for (int e = e0; e < e1; ++e) sa += ctl.aux[e];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(kFullMask, su, o);
-        const double mean = su / double(E);
+        for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(kFullMask, sa, o);
+        float sq = 0.0f;
         for (int e = e0; e < e1; ++e) {
-          const double dv = double(ctl.aux[e]) * (1.0 / 1073741824.0) / S - mean;
-          sq += dv * dv;
+          const float dv = usage_deviation(ctl.aux[e], sa, E, p.S);
+          sq = fmaf(dv, dv, sq);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
-        if (lane == 0) *p.l_aux = okb ? float(sqrt(sq / double(E)) + 1e-6) : NAN;
+        if (lane == 0) *p.l_aux = okb ? sqrtf(sq / float(E)) + 1e-6f : NAN;
       } else {
         // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
-        if (lane == 0) *p.l_aux = okb ? float(double(E) * aux / (S * S)) : NAN;
+        float aux = 0.0f;
+        for (int e = e0; e < e1; ++e)
+          aux = fmaf(float(ctl.aux[e]) * kInvFix30, float(ctl.tot[0][e]), aux);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
+        if (lane == 0) *p.l_aux = okb ? float(E) * aux / S / S : NAN;
       }
     }
   }

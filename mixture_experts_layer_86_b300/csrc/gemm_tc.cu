@@ -40,6 +40,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rng.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -407,17 +408,23 @@ struct __align__(8) PairCtl {
   int tile_start[kMaxGroups + 1];  // prefix of (token tiles x 256-feature tiles)
   int row_start[kMaxGroups + 1];   // the expert offsets, read once from global memory
 };
-// 2 warps per TMEM lane quadrant take alternate 32-token chunks, so the
-// epilogue keeps up with tiles whose K loop is short (d = 512 or 1024)
-constexpr int kPairEpiWarps = 8;
-constexpr int kPairThreads = 32 * (2 + kPairEpiWarps);
+// 3 warps per TMEM lane quadrant take every third 32-token chunk, so the
+// epilogue (bias, activation, one or two stored outputs, or act' for the
+// data gradient) keeps up with tiles whose K loop is short (d = 512 or
+// 1024); the gather form keeps 2 per quadrant (its gather warps take the
+// rest of the register file)
 constexpr int kPairGatherWarps = 4;
-constexpr int kPairThreadsGather = kPairThreads + 32 * kPairGatherWarps;
-constexpr size_t kPairSmemBytes = 1024 + kPairStages * (kPairABytes + kPairBBytes) +
-                                  kPairEpiWarps * kStageBytesPerWarp + sizeof(PairCtl);
+__host__ __device__ constexpr int pair_epi_warps(bool gather) { return gather ? 8 : 12; }
+__host__ __device__ constexpr int pair_threads(bool gather) {
+  return 32 * (2 + pair_epi_warps(gather) + (gather ? kPairGatherWarps : 0));
+}
+constexpr size_t pair_smem_bytes(bool gather) {
+  return 1024 + kPairStages * (kPairABytes + kPairBBytes) +
+         pair_epi_warps(gather) * kStageBytesPerWarp + sizeof(PairCtl);
+}
 
 template <bool kWMN, bool kGather>
-__global__ void __launch_bounds__(kGather ? kPairThreadsGather : kPairThreads, 1)
+__global__ void __launch_bounds__(pair_threads(kGather), 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX,
                     const int32_t *__restrict__ offsets, int64_t dense_rows, int G, int N,
@@ -426,7 +433,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                     const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err,
                     const __nv_bfloat16 *__restrict__ xg, const int32_t *__restrict__ row_src,
-                    int kch) {
+                    int kch, int b_wrap, const TcRouterEpi rt) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -434,7 +441,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   uint8_t *sA = smem;
   uint8_t *sB = smem + kPairStages * kPairABytes;
   uint8_t *sStage = smem + kPairStages * (kPairABytes + kPairBBytes);
-  PairCtl &ctl = *reinterpret_cast<PairCtl *>(sStage + kPairEpiWarps * kStageBytesPerWarp);
+  constexpr int kEpi = pair_epi_warps(kGather), kSub = kEpi / 4;
+  PairCtl &ctl = *reinterpret_cast<PairCtl *>(sStage + kEpi * kStageBytesPerWarp);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -451,7 +459,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl.tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 2 * kPairEpiWarps);  // both CTAs
+      ptx::mbar_init(ptx::smem_addr(&ctl.tempty[a]), 2 * kEpi);  // both CTAs
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
@@ -514,10 +522,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
             if (!kWMN) {
               ptx::tma_load_2d_pair(ptx::smem_addr(a), &tmW, fb, k0, tc.g * N + frow);
             } else {
+              // the router form repeats B's rows every b_wrap (a multiple of 64)
+              const int wrow = b_wrap ? k0 % b_wrap : tc.g * K + k0;
 #pragma unroll
               for (int j = 0; j < kFeat / 64; ++j)
                 ptx::tma_load_2d_pair(ptx::smem_addr(a + j * (64 * 128)), &tmW, fb, frow + j * 64,
-                                      tc.g * K + k0);
+                                      wrow);
             }
             if (!kGather)
               ptx::tma_load_2d_pair(ptx::smem_addr(sB + stage * kPairBBytes + h * kHalfBytes),
@@ -592,11 +602,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       if (!ptx::mbar_wait_cluster(ptx::smem_addr(&ctl.drain), 0, nullptr, kWaitLimitNs))
         record_error(err, kErrGemmDrain);
     }
-  } else if (kGather && warp >= 2 + kPairEpiWarps) {
+  } else if (kGather && warp >= 2 + kEpi) {
     // ------------------- token rows gathered from x (the fused dispatch)
     // this warp's 32 rows of the CTA's half of the token tile, 4 rows per
     // pass: 8 lanes x 16 bytes = one 64-wide K half of a row
-    const int gw = warp - (2 + kPairEpiWarps);
+    const int gw = warp - (2 + kEpi);
     const int c16 = lane & 7, rsub = lane >> 3;
     const uint32_t full_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.full[0]), 0);
     // stages whose copies are in flight, oldest first: up to the whole ring,
@@ -672,7 +682,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   } else if (warp >= 2) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;             // TMEM lane quadrant = this warp's 32 features
-    const int half = (warp - 2) >> 2;   // which alternate 32-token chunks
+    const int sub = (warp - 2) >> 2;    // this warp takes 32-token chunks sub, sub + kSub, ...
     uint8_t *stg = sStage + (warp - 2) * kStageBytesPerWarp;
     const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
@@ -695,7 +705,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * kTok);
       const int nchunk = (tc.ntok + 31) >> 5;
 #pragma unroll 1
-      for (int c = half; c < nchunk; c += 2) {
+      for (int c = sub; c < nchunk; c += kSub) {
         uint32_t raw[32];
         ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
         ptx::tmem_ld_wait();
@@ -704,6 +714,56 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]) + bv;
+        if (kWMN && rt.src) {
+          // router form: x = acc * f(s, n) + the experts' rows of token s
+          const auto *src = static_cast<const __nv_bfloat16 *>(rt.src);
+          int r0 = -1, r1 = -1;  // lane t: the rows of this chunk's token t
+          if (lane < ntk) {
+            r0 = rt.rows[(trow0 + lane) * rt.k];
+            if (rt.k == 2) r1 = rt.rows[(trow0 + lane) * 2 + 1];
+          }
+          if (rt.jitter) {
+            const rng::Key key = rng::make_key(rt.noise.seed, rt.noise.offset);
+            const float eps = rt.noise.jitter_eps > 0.0f ? rt.noise.jitter_eps : 0.01f;
+            // one token per pass; x rotates by one so that only x[0] is
+            // indexed (a rolled loop with static register indices)
+#pragma unroll 1
+            for (int i = 0; i < 32; ++i) {
+              float fac = 1.0f;
+              if (i < ntk) {
+                const uint4 w4 = rng::block(key, rng::kPurposeJitter, uint32_t(trow0 + i),
+                                            uint32_t(f >> 2));
+                fac = rng::jitter(rng::uniform(rng::word(w4, f & 3)), eps);
+              }
+              const float t = x[0] * fac;
+#pragma unroll
+              for (int j = 0; j < 31; ++j) x[j] = x[j + 1];
+              x[31] = t;
+            }
+          }
+          // per choice: the chunk's 32 row segments (32 features, 64 B each)
+          // gathered through the staging tile, 4 16-byte loads in flight per
+          // lane, then added column by column
+#pragma unroll 1
+          for (int j = 0; j < rt.k; ++j) {
+            const int rj = j == 0 ? r0 : r1;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
+              const int row = __shfl_sync(kFullMask, rj, tr);
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (row >= 0 && fc < N)
+                v = *reinterpret_cast<const uint4 *>(src + int64_t(row) * N + fc);
+              *reinterpret_cast<uint4 *>(stg + tr * 64 + pp * 16) = v;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              x[i] += __bfloat162float(
+                  *reinterpret_cast<const __nv_bfloat16 *>(stg + i * 64 + lane * 2));
+            __syncwarp();
+          }
+        }
         if (grad_src) {
 #pragma unroll
           for (int s4 = 0; s4 < 4; ++s4) {
@@ -767,7 +827,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
 // Both operands are MN-major in shared memory.  The last K block of a group
 // may hold rows of the next group (or unwritten rows past the last group):
 // a fixup warp zeroes those rows in shared memory before the MMA reads the
-// stage, so every K block goes producer -> full -> fixup -> ready -> MMA.
+// stage (producer -> full -> fixup -> ready -> MMA); whole K blocks go
+// producer -> full -> MMA.
 // An expert with no rows gets an exact zero tile without touching TMEM.
 // warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue (2 per TMEM lane
 // quadrant, alternate 32-column chunks: a tile's K loop is one expert's
@@ -796,10 +857,26 @@ __device__ __forceinline__ void wg_tile(int t, int mt, int nt, int &g, int &m, i
   m = l - n * mt;
 }
 
+// rows [r0, r0 + rows) of group g: from the offsets, or uniform chunks of
+// `chunk` rows of rows_total when there are none
+__device__ __forceinline__ void wg_group(const int32_t *offsets, int chunk, int64_t rows_total,
+                                         int g, int &r0, int &rows) {
+  if (offsets) {
+    r0 = offsets[g];
+    rows = offsets[g + 1] - r0;
+  } else {
+    const int64_t a = min(int64_t(g) * chunk, rows_total);
+    const int64_t b = min(a + chunk, rows_total);
+    r0 = int(a);
+    rows = int(b - a);
+  }
+}
+
 __global__ void __launch_bounds__(kWgThreads, 1)
 tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const int32_t *__restrict__ offsets, int G, int M, int N,
-                __nv_bfloat16 *__restrict__ C, unsigned int *err) {
+                __nv_bfloat16 *__restrict__ C, unsigned int *err, int chunk, int64_t rows_total,
+                float *__restrict__ Cf) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -845,7 +922,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int g, m, n;
         wg_tile(t, mt, nt, g, m, n);
-        const int r0 = offsets[g], rows = offsets[g + 1] - r0;
+        int r0, rows;
+        wg_group(offsets, chunk, rows_total, g, r0, rows);
         const int nk = (rows + BK - 1) / BK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, kWaitLimitNs)) {
@@ -887,9 +965,17 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       int g, m, n;
       wg_tile(t, mt, nt, g, m, n);
-      const int rows = offsets[g + 1] - offsets[g];
+      int r0, rows;
+      wg_group(offsets, chunk, rows_total, g, r0, rows);
       const int nk = (rows + BK - 1) / BK;
       for (int kb = 0; kb < nk; ++kb) {
+        if (rows - kb * BK >= BK) {  // a whole K block: the MMA takes it directly
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         bool got = true;
         if (lane == 0)
           got = ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, kWaitLimitNs);
@@ -926,17 +1012,20 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, 1, 1);
       const uint64_t a_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sA), BK * 128, 1024);
       const uint64_t b_desc0 = ptx::sdesc_sw128(ptx::smem_addr(sB), BK * 128, 1024);
       int stage = 0, it = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, ready_ph = 0;  // ready completes only on the blocks the fixup takes
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
         int g, m, n;
         wg_tile(t, mt, nt, g, m, n);
-        const int rows = offsets[g + 1] - offsets[g];
+        int r0, rows;
+        wg_group(offsets, chunk, rows_total, g, r0, rows);
         const int nk = (rows + BK - 1) / BK;
+        // N of the MMA: the tile's columns rounded up to a 64-wide swizzle atom
+        const int ncols = min(BN, (min(BN, N - n * BN) + 63) & ~63);
+        const uint32_t idesc = ptx::idesc_bf16(BM, ncols, 1, 1);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tempty[acc]), acc_phase ^ 1u, abort, kWaitLimitNs)) {
@@ -947,7 +1036,11 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.ready[stage]), phase, abort, kWaitLimitNs)) {
+          const bool whole = rows - kb * BK >= BK;
+          const uint32_t bar = ptx::smem_addr(whole ? &ctl.full[stage] : &ctl.ready[stage]);
+          const uint32_t par = whole ? phase : (ready_ph >> stage) & 1u;
+          if (!whole) ready_ph ^= 1u << stage;
+          if (!ptx::mbar_wait(bar, par, abort, kWaitLimitNs)) {
             record_error(err, kErrWgradMma | uint32_t(t & 0x7fffff));
             *abort = 1;
             ok = false;
@@ -981,7 +1074,9 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       int g, m, n;
       wg_tile(t, mt, nt, g, m, n);
-      const bool empty_group = offsets[g + 1] == offsets[g];
+      int r0, rows;
+      wg_group(offsets, chunk, rows_total, g, r0, rows);
+      const bool empty_group = rows == 0;
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!ptx::mbar_wait(ptx::smem_addr(&ctl.tfull[acc]), acc_phase, abort, kWaitLimitNs)) {
@@ -993,6 +1088,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int row = m * BM + r_in_tile;
       const bool valid = row < M;
       __nv_bfloat16 *crow = C + (int64_t(g) * M + row) * N;
+      float *crow_f = Cf + (int64_t(g) * M + row) * N;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
 #pragma unroll 1
       for (int c = half; c < BN / 32; c += 2) {
@@ -1013,7 +1109,12 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           float x[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
-          *reinterpret_cast<uint4 *>(crow + col) = pack_bf16x8(x);
+          if (Cf) {
+            *reinterpret_cast<float4 *>(crow_f + col) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4 *>(crow_f + col + 4) = make_float4(x[4], x[5], x[6], x[7]);
+          } else {
+            *reinterpret_cast<uint4 *>(crow + col) = pack_bf16x8(x);
+          }
         }
       }
       ptx::tc_fence_before();
@@ -1044,13 +1145,14 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 //           hold the next group's rows or unwritten memory and must read as
 //           zero -- or any K block of a first-N tile, whose A columns also
 //           give the bias gradient db_g = sum over rows of A): each CTA's
-//           copies complete on its own `tail` barrier; its warp 10 zeroes
-//           the rows past the group, adds A's columns, fences the stage for
-//           the tensor cores and arrives on the even CTA's `ready` barrier,
-//           which the MMA waits on.
+//           copies complete on its own `tail` barrier; its 4 relay warps
+//           zero the rows past the group (each a quarter of the rows), add
+//           A's valid rows column by column (each a quarter of the
+//           columns), fence the stage for the tensor cores and arrive on
+//           the even CTA's `ready` barrier, which the MMA waits on.
 // Both CTAs walk the same tiles and K blocks, so every role agrees on each
 // stage's path; the phase of each barrier kind is tracked per stage.
-//   both CTAs  warp 0: TMA producer; warp 10: the relay; warps 2..9:
+//   both CTAs  warp 0: TMA producer; warps 10..13: the relay; warps 2..9:
 //              epilogue of this CTA's 128 rows of the tile
 //   even CTA   warp 1: the pair MMAs; commits are multicast to both CTAs'
 //              `empty` / `tfull` barriers.
@@ -1059,8 +1161,9 @@ constexpr int kWpStages = 3;
 constexpr uint32_t kWpBoxBytes = 64 * 64 * 2;               // 64 cols x 64 rows, 8 KB
 constexpr uint32_t kWpOpBytes = 4 * kWpBoxBytes;            // one operand half per stage, 32 KB
 constexpr int kWpEpiWarps = 8;
-constexpr int kWpFixupWarp = 2 + kWpEpiWarps;
-constexpr int kWpThreads = 32 * (kWpFixupWarp + 1);
+constexpr int kWpFixupWarp = 2 + kWpEpiWarps;  // the first relay warp
+constexpr int kWpRelayWarps = 4;
+constexpr int kWpThreads = 32 * (kWpFixupWarp + kWpRelayWarps);
 
 struct __align__(8) WpCtl {
   uint64_t full[kWpStages];    // even CTA: direct stages, both CTAs' bytes
@@ -1073,7 +1176,10 @@ struct __align__(8) WpCtl {
   uint32_t tmem_base;
   int abort;
 };
-constexpr size_t kWpSmemBytes = 1024 + kWpStages * 2 * kWpOpBytes + sizeof(WpCtl);
+// each epilogue warp's bf16 staging tile: 32 rows x 32 columns, 64 B a row
+constexpr uint32_t kWpStgBytes = 32 * 64;
+constexpr size_t kWpSmemBytes =
+    1024 + kWpStages * 2 * kWpOpBytes + kWpEpiWarps * kWpStgBytes + sizeof(WpCtl);
 
 // whether K block kb of a group with `rows` rows goes through the relay
 __device__ __forceinline__ bool wp_relayed(int rows, int kb, bool sum) {
@@ -1095,7 +1201,8 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + kWpStages * kWpOpBytes;
-  WpCtl &ctl = *reinterpret_cast<WpCtl *>(smem + kWpStages * 2 * kWpOpBytes);
+  uint8_t *sStg = smem + kWpStages * 2 * kWpOpBytes;
+  WpCtl &ctl = *reinterpret_cast<WpCtl *>(sStg + kWpEpiWarps * kWpStgBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
@@ -1107,7 +1214,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < kWpStages; ++s) {
       ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl.tail[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 2);  // the relay of each CTA
+      ptx::mbar_init(ptx::smem_addr(&ctl.ready[s]), 2 * kWpRelayWarps);  // both CTAs' relays
       ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -1210,14 +1317,20 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
     }
-  } else if (warp == kWpFixupWarp) {
+  } else if (warp >= kWpFixupWarp) {
     // ------------------------------ the relay of relayed stages (see above)
+    const int rw = warp - kWpFixupWarp;
     int stage = 0;
     uint32_t tail_ph = 0;
     bool ok = true;
     const uint32_t ready_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.ready[0]), 0);
-    // this lane's 4 columns of A (of the CTA's 128): box j, 16-byte chunk, offset
-    const int cj = lane >> 4, cchunk = (lane & 15) >> 1, csub = (lane & 1) * 8;
+    // zeroing: this warp's 32 rows of the 128, in K half zh
+    const int zh = rw >> 1, zr0 = (rw & 1) * 32;
+    // column sums: this warp's 32 of the CTA's 128 columns of A (box cj),
+    // this lane's 4 of them (16-byte chunk cchunk, byte offset csub) over
+    // rows 32 * rg .. 32 * rg + 31 of each stage
+    const int quad = lane & 7, rg = lane >> 3;
+    const int cj = rw >> 1, cchunk = 4 * (rw & 1) + (quad >> 1), csub = (quad & 1) * 8;
     for (int t = cid; t < total && ok; t += ncl) {
       int g, m, n;
       wg_tile(t, mt, nt, g, m, n);
@@ -1243,49 +1356,59 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           ok = false;
           break;
         }
-        const int valid = rows - kb * kWpBK;
+        const int valid = rows - kb * kWpBK;  // rows of this stage inside the group
         if (valid < kWpBK) {
+          // rows [max(valid, 64 zh + zr0), 64 zh + zr0 + 32) of both operands
+          const int vr = max(0, min(32, valid - (64 * zh + zr0)));
+          const int nbytes = (32 - vr) * 128;
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int vr = max(0, min(64, valid - h * 64));  // valid rows of this K half
-            const int nbytes = (64 - vr) * 128;              // contiguous tail of each box
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint32_t off = st * kWpOpBytes + (h * 2 + j) * kWpBoxBytes + vr * 128;
-              for (int i = lane * 16; i < nbytes; i += 32 * 16) {
-                *reinterpret_cast<uint4 *>(sA + off + i) = z;
-                *reinterpret_cast<uint4 *>(sB + off + i) = z;
-              }
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t off =
+                st * kWpOpBytes + (zh * 2 + j) * kWpBoxBytes + (zr0 + vr) * 128;
+            for (int i = lane * 16; i < nbytes; i += 32 * 16) {
+              *reinterpret_cast<uint4 *>(sA + off + i) = z;
+              *reinterpret_cast<uint4 *>(sB + off + i) = z;
             }
           }
         }
-        __syncwarp();
         if (sum) {
-          // rows past the group are zero now: add all 128 rows, in order
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint8_t *box = sA + st * kWpOpBytes + (h * 2 + cj) * kWpBoxBytes;
+          // the valid rows only (the others are being zeroed by the warps
+          // that own them), in row order
+          const int h = rg >> 1, r0 = (rg & 1) * 32;
+          const uint8_t *box = sA + st * kWpOpBytes + (h * 2 + cj) * kWpBoxBytes;
+          const int nr = max(0, min(32, valid - 32 * rg));
 #pragma unroll 4
-            for (int kr = 0; kr < 64; ++kr) {
-              const uint2 v = *reinterpret_cast<const uint2 *>(
-                  box + kr * 128 + ((cchunk ^ (kr & 7)) << 4) + csub);
-              acc[0] += __uint_as_float(v.x << 16);
-              acc[1] += __uint_as_float(v.x & 0xffff0000u);
-              acc[2] += __uint_as_float(v.y << 16);
-              acc[3] += __uint_as_float(v.y & 0xffff0000u);
-            }
+          for (int i = 0; i < nr; ++i) {
+            const int kr = r0 + i;
+            const uint2 v = *reinterpret_cast<const uint2 *>(
+                box + kr * 128 + ((cchunk ^ (kr & 7)) << 4) + csub);
+            acc[0] += __uint_as_float(v.x << 16);
+            acc[1] += __uint_as_float(v.x & 0xffff0000u);
+            acc[2] += __uint_as_float(v.y << 16);
+            acc[3] += __uint_as_float(v.y & 0xffff0000u);
           }
         }
-        ptx::fence_proxy_async_smem();  // this CTA's stage is complete for the MMA's reads
+        ptx::fence_proxy_async_smem();  // this warp's zeroes are visible to the MMA's reads
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_remote(ready_leader + uint32_t(st) * 8u);
       }
       if (sum && ok) {
-        const int col = m * 256 + int(rank) * 128 + cj * 64 + cchunk * 8 + (csub >> 1);
+        // the 4 row groups' sums, in row-group order (lanes q, q+8, q+16, q+24)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (col + c < M) colsum[int64_t(g) * M + col + c] = __float2bfloat16_rn(acc[c]);
+        for (int c = 0; c < 4; ++c) {
+          const float a1 = __shfl_sync(kFullMask, acc[c], quad + 8);
+          const float a2 = __shfl_sync(kFullMask, acc[c], quad + 16);
+          const float a3 = __shfl_sync(kFullMask, acc[c], quad + 24);
+          const float a0 = __shfl_sync(kFullMask, acc[c], quad);
+          acc[c] = ((a0 + a1) + a2) + a3;
+        }
+        const int col = m * 256 + int(rank) * 128 + cj * 64 + cchunk * 8 + (csub >> 1);
+        if (rg == 0) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (col + c < M) colsum[int64_t(g) * M + col + c] = __float2bfloat16_rn(acc[c]);
+        }
       }
     }
   } else if (warp == 1) {
@@ -1353,8 +1476,12 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;             // TMEM lane quadrant
     const int half = (warp - 2) >> 2;   // which alternate 32-column chunks
-    const int r_in_tile = q * 32 + lane;
     const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_addr(&ctl.tempty[0]), 0);
+    // the chunk goes through shared memory so that each store writes 8 rows
+    // x 64 contiguous bytes; 16-byte pieces are swizzled by row so that
+    // neither side of the transpose has bank conflicts
+    uint8_t *stg = sStg + (warp - 2) * kWpStgBytes;
+    const int pr = lane >> 2, pp = lane & 3;
     int it = 0;
     for (int t = cid; t < total; t += ncl, ++it) {
       int g, m, n;
@@ -1369,12 +1496,12 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       }
       ptx::tc_fence_after();
-      const int row = m * 256 + int(rank) * 128 + r_in_tile;
-      const bool valid = row < M;
-      __nv_bfloat16 *crow = C + (int64_t(g) * M + row) * N;
+      const int row0 = m * 256 + int(rank) * 128 + q * 32;  // this warp's first row
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * 256);
 #pragma unroll 1
       for (int c = half; c < 256 / 32; c += 2) {
+        const int n0 = n * 256 + c * 32;
+        if (n0 >= N) break;
         uint32_t raw[32];
         if (!empty_group) {
           ptx::tmem_ld32(tbase + uint32_t(c * 32), raw);
@@ -1383,17 +1510,23 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 32; ++i) raw[i] = 0u;
         }
-        const int n0 = n * 256 + c * 32;
-        if (!valid || n0 >= N) continue;
 #pragma unroll
         for (int v8 = 0; v8 < 4; ++v8) {
-          const int col = n0 + v8 * 8;
-          if (col >= N) break;
           float x[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(raw[v8 * 8 + i]);
-          *reinterpret_cast<uint4 *>(crow + col) = pack_bf16x8(x);
+          *reinterpret_cast<uint4 *>(stg + lane * 64 + ((v8 ^ ((lane >> 1) & 3)) << 4)) =
+              pack_bf16x8(x);
         }
+        __syncwarp();
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int tr = s4 * 8 + pr, row = row0 + tr, col = n0 + pp * 8;
+          if (row < M && col < N)
+            *reinterpret_cast<uint4 *>(C + (int64_t(g) * M + row) * N + col) =
+                *reinterpret_cast<const uint4 *>(stg + tr * 64 + ((pp ^ ((tr >> 1) & 3)) << 4));
+        }
+        __syncwarp();
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -1452,7 +1585,8 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
       !make_bf16_map(&tb, g.B, uint64_t(g.N), uint64_t(g.rows_alloc), 64, BK))
     return cudaErrorInvalidValue;
   const int sms = num_sms();
-  if (sms >= 2) {
+  if (sms >= 2 && !g.single) {
+    if (g.Cf || !g.offsets) return cudaErrorNotSupported;
     // CTA pairs: 256 x 256 tiles, one M half of A and one N half of B per CTA
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attr[1];
@@ -1488,6 +1622,7 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
                               static_cast<__nv_bfloat16 *>(g.colsum), g.err);
   }
   if (g.colsum) return cudaErrorNotSupported;  // the single-CTA kernel has no column sums
+  if (!g.offsets && g.chunk_rows <= 0) return cudaErrorInvalidValue;
   static PerDevice<int> smem_raised;
   int unused = 0;
   if (const cudaError_t e = smem_raised.get(&unused, [](int &) {
@@ -1498,7 +1633,7 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
   const int tiles = g.G * ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_k(tc_wgrad_kernel, grid, kWgThreads, kWgSmemBytes, st, ta, tb, g.offsets, g.G, g.M,
-                  g.N, static_cast<__nv_bfloat16 *>(g.C), g.err);
+                  g.N, static_cast<__nv_bfloat16 *>(g.C), g.err, g.chunk_rows, g.rows_alloc, g.Cf);
 }
 
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
@@ -1510,7 +1645,8 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
   if (g.b_kmajor)
     okw = make_bf16_map(&tw, g.B, uint64_t(g.K), uint64_t(g.G) * g.N, BK, kFeat);
   else
-    okw = make_bf16_map(&tw, g.B, uint64_t(g.N), uint64_t(g.G) * g.K, 64, BK);
+    okw = make_bf16_map(&tw, g.B, uint64_t(g.N),
+                        g.b_wrap ? uint64_t(g.b_rows) : uint64_t(g.G) * g.K, 64, BK);
   if (!okw) return cudaErrorInvalidValue;
 
   const int sms = num_sms();
@@ -1533,8 +1669,8 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    lc.blockDim = dim3(gather ? kPairThreadsGather : kPairThreads);
-    lc.dynamicSmemBytes = kPairSmemBytes;
+    lc.blockDim = dim3(pair_threads(gather));
+    lc.dynamicSmemBytes = pair_smem_bytes(gather);
     lc.stream = st;
     lc.attrs = attr;
     lc.numAttrs = 1;
@@ -1544,7 +1680,7 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
     int npairs = 0;
     const cudaError_t e = resident_pairs[which].get(&npairs, [&](int &v) {
       cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(kPairSmemBytes));
+                                           int(pair_smem_bytes(gather)));
       if (r != cudaSuccess) return r;
       lc.gridDim = dim3(sms & ~1);
       int ncl = 0;
@@ -1561,9 +1697,11 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
                               static_cast<__nv_bfloat16 *>(g.C),
                               static_cast<__nv_bfloat16 *>(g.pre),
                               static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err,
-                              static_cast<const __nv_bfloat16 *>(g.A), g.row_src, g.k_choices);
+                              static_cast<const __nv_bfloat16 *>(g.A), g.row_src, g.k_choices,
+                              g.b_wrap, g.rt);
   }
-  if (g.row_src) return cudaErrorNotSupported;  // the gather form needs CTA pairs
+  if (g.row_src || g.b_wrap || g.rt.src)
+    return cudaErrorNotSupported;  // the gather and router forms need CTA pairs
   static PerDevice<int> smem_raised[2];
   const int which = g.b_kmajor ? 0 : 1;
   auto kern = g.b_kmajor ? tc_gemm_kernel<false> : tc_gemm_kernel<true>;

@@ -187,6 +187,18 @@ cudaError_t launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
 // and row r of the grouped operand is token row_src[r] / k_choices of it
 // (the dispatch copy fused into the GEMM); C, pre and the groups keep the
 // expert-major row order.  Needs b_kmajor and CTA pairs.
+// Router form of the input gradient (rt.src set; one group, !b_kmajor, CTA
+// pairs): row k of B is row k mod b_wrap of a [b_rows, N] matrix (rows past
+// b_rows read as zero), and the epilogue stores, per token row s,
+//   C[s, n] = acc * f(s, n) + sum_j src[rows[s, j], n]
+// over the kept choices (rows[s, j] >= 0), f the jitter factor (1 without).
+struct TcRouterEpi {
+  const void *src;            // [rows, N] bf16: the experts' input-gradient rows
+  const int32_t *rows;        // [S, k]: row of each choice in src, -1 when dropped
+  int k;
+  int jitter;                 // nonzero: multiply acc by the jitter factor
+  RouteNoise noise;
+};
 struct TcGemm {
   const void *A; int64_t rows_alloc;   // rows of the A/C allocations
   const void *B; bool b_kmajor;
@@ -200,6 +212,8 @@ struct TcGemm {
   unsigned int *err;
   const int32_t *row_src;  // gather form: [rows] s*k+j of each row, else null
   int k_choices;
+  int b_wrap, b_rows;      // router form: K rows of B repeat every b_wrap rows (0: off)
+  TcRouterEpi rt;
 };
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 
@@ -208,6 +222,10 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 // A: [rows, M] bf16, B: [rows, N] bf16 (both row-major), C: [G, M, N] bf16.
 // colsum (nullable): [G, M] bf16, the column sums of A over each group's
 // rows (the bias gradient that goes with the weight gradient).
+// Cf (fp32, nullable) replaces C; offsets == null makes group g the rows
+// [g * chunk_rows, min((g + 1) * chunk_rows, rows_alloc)) (a split of one
+// long reduction into partial sums, each written to its own C_g); single
+// takes the one-CTA kernel.
 struct TcWgrad {
   const void *A; const void *B; int64_t rows_alloc;
   void *C;
@@ -215,6 +233,9 @@ struct TcWgrad {
   const int32_t *offsets;
   void *colsum;
   unsigned int *err;
+  float *Cf;
+  int chunk_rows;
+  bool single;
 };
 cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);
 
@@ -236,12 +257,13 @@ cudaError_t launch_residual_mix(const void *x, int dtype, int64_t S, int d,
                                 cudaStream_t st);
 
 // ------------------------------------------------ backward helpers
-// dO[row] = w * dY[s], dw[s,j] = <dY[s], out[row]> (0 when dropped).
+// dO[row] = w * dY[s], dw[s,j] = <dY[s], out[row]> (0 when dropped);
+// rows (nullable): [S, k] the row of each choice, -1 when dropped.
 cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype,
                                int64_t S, int d, int k, const int32_t *idx,
                                const int32_t *slot, const int32_t *offsets,
                                const float *w, void *d_out, float *dw,
-                               cudaStream_t st);
+                               cudaStream_t st, int32_t *rows = nullptr);
 // db[g, n] = sum over group rows of M[r, n]  (zero for empty groups).
 cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
                                 const int32_t *offsets, void *db,
@@ -254,10 +276,30 @@ cudaError_t launch_aux_coef(const int32_t *idx, const float *probs, int64_t S, i
 // dlogits = inv_temp * p * (dp - <dp,p>), dp from dw through the weights
 // and the l_aux term aux_w * coef[e]: the gradient of the logits the gate
 // GEMM produced (before the 1/T scaling).
+// dlogits (fp32, nullable); dl2 (bf16, nullable): [S, 2P] rows holding
+// hi = bf16(dlogits) in columns [0, E) and lo = bf16(dlogits - hi) in
+// [P, P + E), zeros elsewhere -- the tensor-core operand of the router's
+// backward products (hi + lo carries dlogits to about 2^-17).
 cudaError_t launch_gate_bwd(const float *probs, const int32_t *idx,
                             const float *dw, const float *coef, int64_t S,
                             int E, int k, float aux_w, float inv_temp, float *dlogits,
-                            cudaStream_t st);
+                            void *dl2, int P, cudaStream_t st);
+// ---- router backward on the tensor cores (bf16 layers)
+// P = E rounded up to 64: the half width of the [S, 2P] hi/lo operand.
+inline int router_pad(int E) { return (E + 63) / 64 * 64; }
+// dW_g = dlogits^T x as x^T [hi | lo] over token chunks (fp32 partial sums
+// [chunks, d, 2P], one-CTA K-grouped tensor-core GEMM), then a fixed-order
+// sum of the chunks and of the two halves.
+int gate_wgrad_tc_chunks(int64_t S, int d);
+size_t gate_wgrad_tc_partial_bytes(int64_t S, int E, int d);
+cudaError_t launch_gate_wgrad_tc(const void *x, const void *dl2, int64_t S, int d, int E,
+                                 float *partial, void *dw_gate, unsigned int *err,
+                                 cudaStream_t st);
+// dX = [hi | lo] [W_g; W_g] (* jitter factor) + sum_j dx_disp[row(s, j)]: the
+// CTA-pair GEMM with the router epilogue.
+cudaError_t launch_dx_router_tc(const void *dl2, const void *w_gate, const void *dx_disp,
+                                int64_t S, int d, int E, int k, const int32_t *rows, void *dx,
+                                const RouteNoise *jitter, unsigned int *err, cudaStream_t st);
 // dW_g = dlogits^T x: token-split fp32 partial sums, then a fixed-order sum.
 int64_t gate_wgrad_splits(int64_t S);
 size_t gate_wgrad_partial_bytes(int64_t S, int E, int d);

@@ -225,7 +225,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
   __shared__ int32_t s_grp[kScanThreads];
   __shared__ long long s_pgrp[kScanThreads];
   __shared__ int32_t s_tot[2][kMaxExperts];
-  __shared__ double s_aux[kMaxExperts];
+  __shared__ long long s_aux[kMaxExperts];  // sum_s p[s,e] in units of 2^-30
   const int lane = threadIdx.x & 31;
 
   // ---- count columns: exclusive scan over CTAs, in place
@@ -274,7 +274,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
     if (threadIdx.x < E) {
       long long tot = 0;
       for (int gg = 0; gg < G; ++gg) tot += s_pgrp[gg * E + threadIdx.x];
-      s_aux[threadIdx.x] = double(tot) * (1.0 / 1073741824.0);
+      s_aux[threadIdx.x] = tot;
     }
   }
   block_sync();
@@ -284,7 +284,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int local = 0;
-    double aux = 0.0;
+    float aux = 0.0f;
     for (int e = e0; e < e1; ++e) {
       const int r = s_tot[0][e] + (k == 2 ? s_tot[1][e] : 0);
       const int kp = (cap < 0 || r < cap) ? r : int(cap);
@@ -292,7 +292,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
       kept[e] = kp;
       first_cnt[e] = s_tot[0][e];
       local += kp;
-      aux += s_aux[e] * double(s_tot[0][e]);
+      aux = fmaf(float(s_aux[e]) * kInvFix30, float(s_tot[0][e]), aux);
     }
     int incl = local;
 #pragma unroll
@@ -310,22 +310,24 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
     if (aux_type == MOE_AUX_STD) {
-      // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
-      double su = 0.0, sq = 0.0;
-      for (int e = e0; e < e1; ++e) su += S > 0 ? s_aux[e] / double(S) : 0.0;
+      // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std);
+      // fp32 from the exact integer sums (no FP64)
+      long long sa = 0;
+      for (int e = e0; e < e1; ++e) sa += s_aux[e];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(kFullMask, su, o);
-      const double mean = su / double(E);
-      for (int e = e0; e < e1; ++e) {
-        const double dv = (S > 0 ? s_aux[e] / double(S) : 0.0) - mean;
-        sq += dv * dv;
-      }
+      for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(kFullMask, sa, o);
+      float sq = 0.0f;
+      if (S > 0)
+        for (int e = e0; e < e1; ++e) {
+          const float dv = usage_deviation(s_aux[e], sa, E, S);
+          sq = fmaf(dv, dv, sq);
+        }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
-      if (lane == 0) *l_aux = float(sqrt(sq / double(E)) + 1e-6);
+      if (lane == 0) *l_aux = sqrtf(sq / float(E)) + 1e-6f;
     } else {
       // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
-      if (lane == 0) *l_aux = S > 0 ? float(double(E) * aux / (double(S) * double(S))) : 0.0f;
+      if (lane == 0) *l_aux = S > 0 ? float(E) * aux / float(S) / float(S) : 0.0f;
     }
   }
 }

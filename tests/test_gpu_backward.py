@@ -57,6 +57,23 @@ def test_backward_odd_widths():
     print("odd widths", _check_all(run, ref, gref))
 
 
+@pytest.mark.parametrize("S,d,f,E,k", [(1200, 128, 64, 256, 2), (900, 2048, 256, 64, 2),
+                                        (333, 512, 128, 8, 1), (5, 64, 64, 4, 2)])
+def test_backward_router_shapes(S, d, f, E, k):
+    """The router's tensor-core backward (dW_g over token chunks, dX with the
+    experts' rows added in the GEMM epilogue) at expert counts whose [hi | lo]
+    operand spans one to eight 64-wide blocks, hidden sizes of one to sixteen
+    128-column tiles, and a batch smaller than one 64-row K block."""
+    wl = Workload(f"router_e{E}", S, d, f, E, k, 1.25, 4, True, "gelu_tanh", "bf16", seed=21,
+                  bias_std=0.1, aux_loss_weight=0.01, backward=True)
+    run = GpuRun(wl, training=True)
+    run.backward()
+    assert N.moe_get_device_error() == 0
+    ref, gref = _oracle_grads(run)
+    check_routing_equal(run, ref)
+    print("router shapes", S, d, E, {k_: f"{v['rel_l2']:.2e}" for k_, v in _check_all(run, ref, gref).items()})
+
+
 def test_backward_empty_expert_gets_zero_gradient():
     wl = WORKLOADS["train_e32"].scaled(400, bias_std=0.1, backward=True, skew=0.0)
     inp = make_inputs(wl)
