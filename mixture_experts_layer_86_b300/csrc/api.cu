@@ -3,6 +3,8 @@
 // The entry points and their contracts are documented in moe_b300.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "moe_b300.h"
@@ -126,7 +128,10 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const size_t eb = elem_bytes(c->dtype);
   const int64_t S = c->num_tokens;
   const bool tc = c->dtype == MOE_BF16;
-  const size_t sz[9] = {align256(size_t(R) * c->hidden_size * eb),
+  // slot 0 (dO) also holds the router term r [S, d] fp32 of bf16 layers,
+  // which is formed after the last use of dO
+  const size_t sz[9] = {align256(std::max(size_t(R) * c->hidden_size * eb,
+                                          tc ? size_t(S) * c->hidden_size * 4 : size_t(0))),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
                         align256(size_t(S) * c->k * 4),
@@ -688,7 +693,8 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     // with the experts' rows added in the GEMM's epilogue
     MOE_CUDA(launch_gate_wgrad_tc(xr, dl2, S, d, E, w.gate_partial, dw_gate,
                                   device_error_ptr(), st));
-    return cuda_status(launch_dx_router_tc(dl2, w_gate, w.dx_disp, S, d, E, k, w.rows, dx, jit,
+    return cuda_status(launch_dx_router_tc(dl2, w_gate, w.dx_disp, S, d, E, k, w.rows,
+                                           static_cast<float *>(w.d_out), dx, jit,
                                            device_error_ptr(), st));
   }
   MOE_CUDA(launch_gate_wgrad(w.dlogits, xr, dt, S, d, E, w.gate_partial, dw_gate, st));

@@ -221,6 +221,50 @@ gate_wgrad_tc_reduce_kernel(const float *__restrict__ part, int nchunk, int d, i
     store_elem(dw_gate, dtype, int64_t(eo) * d + co, tile[threadIdx.x >> 3][threadIdx.x & 7]);
 }
 
+// ------------------------------------------------- dX from the router term
+// dX[s] = r[s] * f(s, .) + sum_j dx_disp[rows[s, j]]; one warp per token,
+// lanes over 8-feature vectors (16 bytes of bf16, 32 of fp32).
+constexpr int kDxrWarps = 8;
+
+__global__ void __launch_bounds__(kDxrWarps * 32)
+dx_router_combine_kernel(const float *__restrict__ rterm, const uint4 *__restrict__ dx_disp,
+                         const int32_t *__restrict__ rows, int64_t S, int nvec, int k,
+                         uint4 *__restrict__ dx, int jitter, RouteNoise noise) {
+  griddep_begin();
+  const int lane = threadIdx.x & 31;
+  const int64_t s = int64_t(blockIdx.x) * kDxrWarps + (threadIdx.x >> 5);
+  if (s >= S) return;
+  const int r0 = rows[s * k], r1 = k == 2 ? rows[s * k + 1] : -1;
+  const float4 *rt = reinterpret_cast<const float4 *>(rterm) + s * nvec * 2;
+  const rng::Key key = rng::make_key(noise.seed, noise.offset);
+  const float eps = noise.jitter_eps > 0.0f ? noise.jitter_eps : 0.01f;
+  for (int c = lane; c < nvec; c += 32) {
+    const float4 a = __ldcs(rt + 2 * c), b = __ldcs(rt + 2 * c + 1);
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (jitter) {
+      // the router's input was x * f: its gradient is the router term * f
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 w4 = rng::block(key, rng::kPurposeJitter, uint32_t(s), uint32_t(2 * c + h));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[4 * h + q] *= rng::jitter(rng::uniform(rng::word(w4, q)), eps);
+      }
+    }
+    float g[8];
+    if (r0 >= 0) {
+      Vec<__nv_bfloat16>::to_f32(dx_disp[int64_t(r0) * nvec + c], g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += g[i];
+    }
+    if (r1 >= 0) {
+      Vec<__nv_bfloat16>::to_f32(dx_disp[int64_t(r1) * nvec + c], g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += g[i];
+    }
+    dx[s * nvec + c] = Vec<__nv_bfloat16>::from_f32(v);
+  }
+}
+
 }  // namespace
 
 // token chunks of the dW_g product: as many (chunk, 128-column) tiles as
@@ -263,19 +307,22 @@ cudaError_t launch_gate_wgrad_tc(const void *x, const void *dl2, int64_t S, int 
 }
 
 cudaError_t launch_dx_router_tc(const void *dl2, const void *w_gate, const void *dx_disp,
-                                int64_t S, int d, int E, int k, const int32_t *rows, void *dx,
-                                const RouteNoise *jitter, unsigned int *err, cudaStream_t st) {
+                                int64_t S, int d, int E, int k, const int32_t *rows,
+                                float *rterm, void *dx, const RouteNoise *jitter,
+                                unsigned int *err, cudaStream_t st) {
   if (S <= 0) return cudaSuccess;
   const int P = router_pad(E);
   TcGemm g{};
-  g.A = dl2; g.rows_alloc = S; g.B = w_gate; g.b_kmajor = false; g.C = dx;
+  g.A = dl2; g.rows_alloc = S; g.B = w_gate; g.b_kmajor = false; g.C = nullptr;
   g.N = d; g.K = 2 * P; g.G = 1; g.offsets = nullptr; g.bias = nullptr; g.act = -1;
   g.pre = nullptr; g.grad_src = nullptr; g.dact = 0; g.err = err;
-  g.b_wrap = P; g.b_rows = E;
-  g.rt.src = dx_disp; g.rt.rows = rows; g.rt.k = k;
-  g.rt.jitter = jitter ? 1 : 0;
-  if (jitter) g.rt.noise = *jitter;
-  return launch_tc_gemm(g, st);
+  g.b_wrap = P; g.b_rows = E; g.c_f32 = rterm;
+  if (const cudaError_t e = launch_tc_gemm(g, st); e != cudaSuccess) return e;
+  const RouteNoise nz = jitter ? *jitter : RouteNoise{};
+  return launch_k(dx_router_combine_kernel, unsigned((S + kDxrWarps - 1) / kDxrWarps),
+                  kDxrWarps * 32, 0, st, static_cast<const float *>(rterm),
+                  static_cast<const uint4 *>(dx_disp), rows, S, d / 8, k,
+                  static_cast<uint4 *>(dx), jitter ? 1 : 0, nz);
 }
 
 int64_t gate_wgrad_splits(int64_t S) {

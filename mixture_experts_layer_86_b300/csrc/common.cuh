@@ -63,6 +63,13 @@ __device__ __forceinline__ float act_grad(float z, int act) {
 constexpr float kFix30 = 1073741824.0f;        // 2^30
 constexpr float kInvFix30 = 9.313225746154785e-10f;  // 2^-30
 
+// a probability sum of at most 2^7 tokens in units of 2^-30, converted
+// through a 32-bit integer at 2^-23 (64-bit float-to-integer conversions are
+// slow on this GPU); the sums stay exact integers
+__device__ __forceinline__ long long fix30_tile(float v) {
+  return static_cast<long long>(__float2int_rn(v * 8388608.0f)) << 7;
+}
+
 // signed 128-bit integer to the nearest-ish float (two roundings)
 __device__ __forceinline__ float i128_to_float(__int128 v) {
   const bool neg = v < 0;

@@ -213,7 +213,8 @@ __global__ void aux_coef_kernel(const int32_t *__restrict__ idx, const float *__
     const int e = threadIdx.x % E, grp = threadIdx.x / E;
     if (grp < G) {
       long long acc = 0;
-      for (int64_t s = grp; s < S; s += G) acc += __float2ll_rn(probs[s * E + e] * kFix30);
+      // p <= 1, so p * 2^30 fits a 32-bit integer
+      for (int64_t s = grp; s < S; s += G) acc += __float2int_rn(probs[s * E + e] * kFix30);
       s_part[grp * E + e] = acc;
     }
     __syncthreads();

@@ -8,33 +8,34 @@
 // ceil(S*2/E*cf)); deepspeed.moe overview (adg.csdn.net/694deb285b9f5f31781ae763)
 // §2.1 (min_capacity, drop_tokens, gate_loss, expert_count).
 //
-// The stage is bound by reading x once from HBM.  Every CTA takes one tile
-// of TM tokens, TM = ceil(S / #SMs) rounded up to 8 rows (at most 128), so
-// every SM streams its share of x at the same time; the kernel is launched
-// cooperatively (all CTAs resident), one CTA per SM.
+// The stage is bound by reading x once from HBM.  Every CTA but the last
+// takes one tile of TM tokens, TM = ceil(S / (#SMs - 1)) rounded up to 8 rows
+// (at most 128), so every SM streams its share of x at the same time; the
+// kernel is launched cooperatively (all CTAs resident), one CTA per SM.
 //
 // Phase A, per tile:
 //   warp 0     TMA producer: x tile (TM x 64 per box) and W_g tile
-//              (E x 64 per box) K-slices into a shared-memory ring
+//              (E x 64 per box) K-slices into a shared-memory ring; the
+//              first pass over the ring is issued during the setup
 //   warp 1     TMEM allocator + MMA issuer: tcgen05.mma M = 128 (rows
 //              past TM are zero), N = E rounded up to 16, fp32 in TMEM
-//   warps 4-7  one token per thread, its logits read straight from TMEM
-//              (lane = token): top-2 with ties to the lower expert index,
-//              softmax of logits / T, combine weights; the tile's
-//              per-expert probability sums (column sums through a
-//              shared-memory transpose, fixed order); per (choice j,
-//              expert e) the tile's count and each token's rank among the
-//              tile's tokens with the same (j, e), in token order
-//              (__match_any_sync within a warp, warp prefixes across).
+//   all warps  epilogue: warp w reads TMEM lane quadrant w % 4 (32 tokens)
+//              and every other 32-expert chunk; top-2 with ties to the
+//              lower expert index, softmax of logits / T, combine weights;
+//              the tile's per-expert probability sums (column sums through
+//              a shared-memory transpose, fixed order)
+//   warps 4-7  per (choice j, expert e) the tile's count and each token's
+//              rank among the tile's tokens with the same (j, e), in token
+//              order (__match_any_sync within a warp, warp prefixes across)
 //   The tile's counts and probability sums go to the workspace.
-// Grid barrier (bounded wait).
-// Phase B, every CTA for its own tile, in parallel: the counts of all
+// Grid barrier (bounded wait), which the last CTA joins straight away.
+// Phase B, every tile CTA for its own tile, in parallel: the counts of all
 //   tiles give this tile's prefix (the tiles before it) and the totals;
 //   slot = prefix[j][e] + (j == 1 ? first-choice total of e : 0) + rank,
 //   dropped at >= capacity.  Every first choice therefore precedes every
 //   second choice, each in token order (the GShard priority order of the
-//   layer's specification).  Tile 0 writes the routed / kept counts, the
-//   expert offsets (exclusive scan of kept) and l_aux.
+//   layer's specification).  Meanwhile the last CTA writes the routed /
+//   kept counts, the expert offsets (exclusive scan of kept) and l_aux.
 // Everything is deterministic: integer counts, probability sums added in
 // a fixed order and then as exact 2^-30 fixed-point integers.
 #include <cuda.h>
@@ -76,9 +77,7 @@ constexpr int kGrMaxTile = 128;
 constexpr uint32_t kXBoxBytes = 128 * 128;      // 128 token rows x 64 bf16; TM rows loaded
 constexpr uint32_t kStgFloats = 32 * 33;        // one epilogue warp's transpose tile
 constexpr uint64_t kGrWaitNs = 2000000000ull;   // 2 s
-#ifndef MOE_GATE_BOXES
-#define MOE_GATE_BOXES 1                        // 64-wide K boxes per ring stage
-#endif
+constexpr int kGrMaxBoxes = 4;                 // 64-wide K boxes per ring stage, at most
 
 struct __align__(16) GrCtl {
   uint64_t full[kGrMaxStages];
@@ -197,316 +196,323 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   const uint32_t wbox_bytes = uint32_t(p.E_pad) * 128;
   const uint64_t lim = g_gate_wait_limit_ns;
 
-  // ---------------------------------------------------------------- setup
-  if (tid == 0) {
-    for (int s = 0; s < p.nstages; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
-    }
-    ptx::mbar_init(ptx::smem_addr(&ctl.done), 1);
-    ctl.abort = 0;
-    ptx::fence_mbar_init();
-    // the first pass over the ring needs no empty slot: its copies start
-    // now, while the other warps set up (they write only the bytes past the
-    // TM rows of each x box, which the copies never touch)
-    for (int kb = 0; kb < p.nstages; ++kb) issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), p.tmem_cols);
-    ptx::tmem_relinquish();
-  }
-  // the [E] bias, and zeros in the x-box rows past TM that the M = 128 MMA
-  // reads (written once; the TMA copies never touch them)
-  for (int e = tid; e < kMaxExperts; e += kGrThreads)
-    ctl.bias[e] = (p.logit_bias != nullptr && p.bias_ld == 0 && e < E) ? p.logit_bias[e] : 0.0f;
-  if (p.TM < kGrMaxTile) {
-    const uint32_t pad = (kGrMaxTile - p.TM) * 128;  // bytes past the TM rows of one box
-    const uint32_t per_box = pad / 16;
-    const uint32_t n = uint32_t(p.nstages * p.nbox) * per_box;
-    for (uint32_t i = tid; i < n; i += kGrThreads) {
-      const uint32_t box = i / per_box, off = (i - box * per_box) * 16;
-      const uint32_t st = box / p.nbox, b = box - st * p.nbox;
-      *reinterpret_cast<uint4 *>(ring + st * p.stage_bytes + b * kXBoxBytes + p.TM * 128 + off) =
-          make_uint4(0, 0, 0, 0);
-    }
-    ptx::fence_proxy_async_smem();  // visible to the tensor cores' reads
-  }
-  ptx::tc_fence_before();
-  block_sync();
-  ptx::tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
-  volatile int *abort = &ctl.abort;
-
-  // ------------------------------------------------------------ phase A
-  if (warp == 0) {
-    if (lane == 0) {
-      // stages 0 .. nstages-1 were issued during the setup (phase 0)
-      uint32_t armed = (1u << p.nstages) - 1u, armed_phase = 0;
-      bool ok = true;
-      for (int kb = p.nstages; kb < p.nk; ++kb) {
-        const int stage = kb % p.nstages;
-        const uint32_t phase = (kb / p.nstages) & 1;
-        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, lim)) {
-          record_error(p.err, kErrGateProducer | uint32_t(tile & 0xffffff));
-          *abort = 1;
-          ok = false;
-          break;
-        }
-        issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
-        armed |= 1u << stage;
-        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+  // Phase A for the tiles; the last CTA has no tile: it only meets the
+  // others at the grid barrier and then publishes the counts, the offsets
+  // and l_aux while they assign their slots.
+  if (tile < p.ntiles) {
+    // ---------------------------------------------------------------- setup
+    if (tid == 0) {
+      for (int s = 0; s < p.nstages; ++s) {
+        ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+        ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
       }
-      if (!ok)  // copies already issued land before the ring is reused
-        for (int s = 0; s < p.nstages; ++s)
-          if (armed & (1u << s))
-            ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
-                           kGrWaitNs / 4);
+      ptx::mbar_init(ptx::smem_addr(&ctl.done), 1);
+      ctl.abort = 0;
+      ptx::tma_prefetch_desc(&tmX);
+      ptx::tma_prefetch_desc(&tmW);
+      ptx::fence_mbar_init();
+      // the first pass over the ring needs no empty slot: its copies start
+      // now, while the other warps set up (they write only the bytes past the
+      // TM rows of each x box, which the copies never touch)
+      for (int kb = 0; kb < p.nstages; ++kb) issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint64_t desc0 = ptx::sdesc_sw128(ptx::smem_addr(ring), 16, 1024);
-      bool ok = true;
-      for (int kb = 0; kb < p.nk; ++kb) {
-        const int stage = kb % p.nstages;
-        const uint32_t phase = (kb / p.nstages) & 1;
-        if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, lim)) {
-          record_error(p.err, kErrGateMma | uint32_t(tile & 0xffffff));
-          *abort = 1;
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
-        const uint64_t sdesc = ptx::sdesc_add(desc0, stage * p.stage_bytes);
-        for (int b = 0; b < nb; ++b) {
-          const uint64_t ad = ptx::sdesc_add(sdesc, b * kXBoxBytes);
-          const uint64_t bd = ptx::sdesc_add(sdesc, p.nbox * kXBoxBytes + b * wbox_bytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16(tmem, ptx::sdesc_add(ad, kk * 32), ptx::sdesc_add(bd, kk * 32), p.idesc,
-                          (kb | b | kk) != 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
-      }
-      ptx::mma_commit(ptx::smem_addr(&ctl.done));
-      // after a give-up, the MMAs already issued finish before TMEM is freed
-      if (!ok) ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, nullptr, kGrWaitNs / 4);
+    if (warp == 1) {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), p.tmem_cols);
+      ptx::tmem_relinquish();
     }
-  }
-
-  // ---------------------------------------------- epilogue: all 8 warps
-  // Warp w reads TMEM lane quadrant q = w % 4 (tokens 32q .. 32q+31 of the
-  // tile) and the expert chunks c = h, h + 2, ... (h = w / 4) of 32 experts
-  // each.  Per chunk the logits (+ bias) go to a 32 x 33 shared tile, whose
-  // rows are tokens and columns experts, so that logits, then exp(l - m),
-  // then probabilities live in the same tile; the two warps of a quadrant
-  // merge their top-2 candidates, maxima and sums through shared memory in a
-  // fixed order.  The ring is idle once every MMA is done.
-  __syncwarp();
-  {
-    const int q = warp & 3, h = warp >> 2;
-    const int r = q * 32 + lane;  // token row of the tile
-    const int64_t s = tok0 + r;
-    const bool valid = r < p.TM && s < p.S;
-    if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, lim)) {
-      record_error(p.err, kErrGateEpilogue | uint32_t(tile & 0xffffff));
-      *abort = 1;
-    }
-    ptx::tc_fence_after();
-    const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-    const float *brow = (p.logit_bias != nullptr && p.bias_ld != 0 && valid)
-                            ? p.logit_bias + s * p.bias_ld
-                            : nullptr;
-    const int nchunk = (E + 31) >> 5;
-    const int my_chunks = (nchunk - h + 1) >> 1;  // chunks h, h+2, ...
-    float *stg0 = reinterpret_cast<float *>(ring) + (warp * p.chunks_per_warp) * kStgFloats;
-    const int64_t wrow0 = tok0 + q * 32;  // first token of this warp's rows
-    int64_t wr = p.S - wrow0;              // valid rows of this warp (<= 0: none)
-    if (wr > p.TM - q * 32) wr = p.TM - q * 32;
-    const int wrows = wr > 32 ? 32 : int(wr);
-
-    // pass 1: logits (+ bias) into the shared tiles; top-2 candidates
-    float b1 = -INFINITY, b2 = -INFINITY;
-    int i1 = -1, i2 = -1;
-    for (int ci = 0; ci < my_chunks; ++ci) {
-      const int c = h + 2 * ci;
-      float *stg = stg0 + ci * kStgFloats;
-      uint32_t raw[32];
-      ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        const int e = c * 32 + t;
-        if (e < E) {
-          const float v = __uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]);
-          if (i1 < 0 || v > b1) {
-            b2 = b1;
-            i2 = i1;
-            b1 = v;
-            i1 = e;
-          } else if (i2 < 0 || v > b2) {
-            b2 = v;
-            i2 = e;
-          }
-          stg[lane * 33 + t] = v;
-        }
+    // the [E] bias, and zeros in the x-box rows past TM that the M = 128 MMA
+    // reads (written once; the TMA copies never touch them)
+    for (int e = tid; e < kMaxExperts; e += kGrThreads)
+      ctl.bias[e] = (p.logit_bias != nullptr && p.bias_ld == 0 && e < E) ? p.logit_bias[e] : 0.0f;
+    if (p.TM < kGrMaxTile) {
+      const uint32_t pad = (kGrMaxTile - p.TM) * 128;  // bytes past the TM rows of one box
+      const uint32_t per_box = pad / 16;
+      const uint32_t n = uint32_t(p.nstages * p.nbox) * per_box;
+      for (uint32_t i = tid; i < n; i += kGrThreads) {
+        const uint32_t box = i / per_box, off = (i - box * per_box) * 16;
+        const uint32_t st = box / p.nbox, b = box - st * p.nbox;
+        *reinterpret_cast<uint4 *>(ring + st * p.stage_bytes + b * kXBoxBytes + p.TM * 128 + off) =
+            make_uint4(0, 0, 0, 0);
       }
-      if (p.logits) {  // coalesced rows of the logits
-        __syncwarp();
-        const int e = c * 32 + lane;
-        for (int rr = 0; rr < wrows; ++rr)
-          if (e < E) p.logits[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
-      }
+      ptx::fence_proxy_async_smem();  // visible to the tensor cores' reads
     }
     ptx::tc_fence_before();
-    ctl.cand_v[h][r][0] = b1;
-    ctl.cand_v[h][r][1] = b2;
-    ctl.cand_i[h][r][0] = i1;
-    ctl.cand_i[h][r][1] = i2;
     block_sync();
-    // the row's top-2 over both halves: ranked by value, ties to the lower
-    // expert index (each half's candidates come in that order already)
-    {
-      const float ov1 = ctl.cand_v[h ^ 1][r][0], ov2 = ctl.cand_v[h ^ 1][r][1];
-      const int oi1 = ctl.cand_i[h ^ 1][r][0], oi2 = ctl.cand_i[h ^ 1][r][1];
-      auto before = [](float av, int ai, float bv, int bi) {
-        return ai >= 0 && (bi < 0 || av > bv || (av == bv && ai < bi));
-      };
-      if (before(ov1, oi1, b1, i1)) {
-        if (before(b1, i1, ov2, oi2)) {
-          b2 = b1;
-          i2 = i1;
-        } else {
-          b2 = ov2;
-          i2 = oi2;
-        }
-        b1 = ov1;
-        i1 = oi1;
-      } else if (before(ov1, oi1, b2, i2)) {
-        b2 = ov1;
-        i2 = oi1;
-      }
-    }
-    const float m = b1;  // the top-1 logit is the softmax shift
-    // pass 2: exp((l - m) / T) in place; this half's sum
-    float z = 0.0f;
-    for (int ci = 0; ci < my_chunks; ++ci) {
-      const int c = h + 2 * ci;
-      float *stg = stg0 + ci * kStgFloats;
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        if (c * 32 + t < E) {
-          const float ev = expf((stg[lane * 33 + t] - m) * p.inv_temp);
-          stg[lane * 33 + t] = ev;
-          z += ev;
-        }
-      }
-    }
-    ctl.zpart[h][r] = z;
-    block_sync();
-    const float inv_z = 1.0f / (ctl.zpart[0][r] + ctl.zpart[1][r]);
-    // pass 3: probabilities (0 past the batch), column sums over the tile's
-    // rows in a fixed order, the optional probability rows
-    for (int ci = 0; ci < my_chunks; ++ci) {
-      const int c = h + 2 * ci;
-      float *stg = stg0 + ci * kStgFloats;
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (c * 32 + t < E) stg[lane * 33 + t] = valid ? stg[lane * 33 + t] * inv_z : 0.0f;
-      __syncwarp();
-      const int e = c * 32 + lane;
-      float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows rr = 4 i + u, fixed order
-#pragma unroll
-      for (int rr = 0; rr < 32; rr += 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cs[u] += stg[(rr + u) * 33 + lane];
-      }
-      if (e < E) ctl.psum_w[q][e] = (cs[0] + cs[1]) + (cs[2] + cs[3]);
-      if (p.probs)
-        for (int rr = 0; rr < wrows; ++rr)
-          if (e < E) p.probs[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
-      __syncwarp();
-    }
-    if (h == 0) {
-      if (valid) {
-        p.idx[s * k] = i1;
-        if (k == 1) {
-          p.w[s] = inv_z;  // exp(l1 - max) = 1
-        } else {
-          const float x2 = expf((b2 - m) * p.inv_temp);
-          const float den = 1.0f + x2;
-          p.w[s * 2] = 1.0f / den;
-          p.w[s * 2 + 1] = x2 / den;
-          p.idx[s * 2 + 1] = i2;
-        }
-      }
-      ctl.choice[0][r] = valid ? i1 : -1;
-      ctl.choice[1][r] = (valid && k == 2) ? i2 : -1;
-    }
-  }
-  block_sync();
-
-  if (warp >= 4) {
-    // the tile's count and each token's rank per (j, e), in token order:
-    // within a warp by __match_any_sync, across the 4 warps by their counts'
-    // prefix; both choices at once, the counts in the ring (idle now)
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int et = tid - 128;  // 0..127 over warps 4..7
-    int32_t *wc = reinterpret_cast<int32_t *>(ring);  // [k][4][E]
-    for (int i = et; i < k * 4 * E; i += 128) wc[i] = 0;
-    epi_sync();
-    int ej[2], rk[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      ej[j] = j < k ? ctl.choice[j][r] : -1;
-      const unsigned peers = __match_any_sync(kFullMask, ej[j]);
-      rk[j] = __popc(peers & lanemask_lt());
-      if (ej[j] >= 0 && rk[j] == 0) wc[(j * 4 + q) * E + ej[j]] = __popc(peers);
-    }
-    epi_sync();
-    for (int i = et; i < k * E; i += 128) {
-      const int j = i / E, ee = i - j * E;
-      int run = 0;
-      for (int w4 = 0; w4 < 4; ++w4) {
-        const int cnum = wc[(j * 4 + w4) * E + ee];
-        wc[(j * 4 + w4) * E + ee] = run;
-        run += cnum;
-      }
-      ctl.cnt[j][ee] = run;
-    }
-    epi_sync();
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-      if (j < k) ctl.rank[j][r] = ej[j] >= 0 ? wc[(j * 4 + q) * E + ej[j]] + rk[j] : 0;
-  } else {
-    // publish the tile's probability sums (padding entries 0)
-    for (int e = tid; e < p.psum_pitch; e += 128)
-      p.psum[int64_t(tile) * p.psum_pitch + e] =
-          e < E ? ((ctl.psum_w[0][e] + ctl.psum_w[1][e]) + ctl.psum_w[2][e]) + ctl.psum_w[3][e]
-                : 0.0f;
-  }
-  block_sync();
-  // publish the tile's counts (padding entries 0)
-  for (int i = tid; i < p.hist_pitch; i += kGrThreads)
-    p.hist[int64_t(tile) * p.hist_pitch + i] = i < k * E ? ctl.cnt[i / E][i % E] : 0;
-
-  ptx::tc_fence_before();
-  block_sync();
-  if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, p.tmem_cols);
+    const uint32_t tmem = ctl.tmem_base;
+    volatile int *abort = &ctl.abort;
+
+    // ------------------------------------------------------------ phase A
+    if (warp == 0) {
+      if (lane == 0) {
+        // stages 0 .. nstages-1 were issued during the setup (phase 0)
+        uint32_t armed = (1u << p.nstages) - 1u, armed_phase = 0;
+        bool ok = true;
+        for (int kb = p.nstages; kb < p.nk; ++kb) {
+          const int stage = kb % p.nstages;
+          const uint32_t phase = (kb / p.nstages) & 1;
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.empty[stage]), phase ^ 1u, abort, lim)) {
+            record_error(p.err, kErrGateProducer | uint32_t(tile & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          issue_stage(p, &tmX, &tmW, ring, ctl, kb, tok0);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+        }
+        if (!ok)  // copies already issued land before the ring is reused
+          for (int s = 0; s < p.nstages; ++s)
+            if (armed & (1u << s))
+              ptx::mbar_wait(ptx::smem_addr(&ctl.full[s]), (armed_phase >> s) & 1u, nullptr,
+                             kGrWaitNs / 4);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint64_t desc0 = ptx::sdesc_sw128(ptx::smem_addr(ring), 16, 1024);
+        bool ok = true;
+        for (int kb = 0; kb < p.nk; ++kb) {
+          const int stage = kb % p.nstages;
+          const uint32_t phase = (kb / p.nstages) & 1;
+          if (!ptx::mbar_wait(ptx::smem_addr(&ctl.full[stage]), phase, abort, lim)) {
+            record_error(p.err, kErrGateMma | uint32_t(tile & 0xffffff));
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int nb = min(p.nbox, p.nk64 - kb * p.nbox);
+          const uint64_t sdesc = ptx::sdesc_add(desc0, stage * p.stage_bytes);
+          for (int b = 0; b < nb; ++b) {
+            const uint64_t ad = ptx::sdesc_add(sdesc, b * kXBoxBytes);
+            const uint64_t bd = ptx::sdesc_add(sdesc, p.nbox * kXBoxBytes + b * wbox_bytes);
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_bf16(tmem, ptx::sdesc_add(ad, kk * 32), ptx::sdesc_add(bd, kk * 32), p.idesc,
+                            (kb | b | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl.empty[stage]));
+        }
+        ptx::mma_commit(ptx::smem_addr(&ctl.done));
+        // after a give-up, the MMAs already issued finish before TMEM is freed
+        if (!ok) ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, nullptr, kGrWaitNs / 4);
+      }
+    }
+
+    // ---------------------------------------------- epilogue: all 8 warps
+    // Warp w reads TMEM lane quadrant q = w % 4 (tokens 32q .. 32q+31 of the
+    // tile) and the expert chunks c = h, h + 2, ... (h = w / 4) of 32 experts
+    // each.  Per chunk the logits (+ bias) go to a 32 x 33 shared tile, whose
+    // rows are tokens and columns experts, so that logits, then exp(l - m),
+    // then probabilities live in the same tile; the two warps of a quadrant
+    // merge their top-2 candidates, maxima and sums through shared memory in a
+    // fixed order.  The ring is idle once every MMA is done.
+    __syncwarp();
+    {
+      const int q = warp & 3, h = warp >> 2;
+      const int r = q * 32 + lane;  // token row of the tile
+      const int64_t s = tok0 + r;
+      const bool valid = r < p.TM && s < p.S;
+      if (!ptx::mbar_wait(ptx::smem_addr(&ctl.done), 0, abort, lim)) {
+        record_error(p.err, kErrGateEpilogue | uint32_t(tile & 0xffffff));
+        *abort = 1;
+      }
+      ptx::tc_fence_after();
+      const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+      const float *brow = (p.logit_bias != nullptr && p.bias_ld != 0 && valid)
+                              ? p.logit_bias + s * p.bias_ld
+                              : nullptr;
+      const int nchunk = (E + 31) >> 5;
+      const int my_chunks = (nchunk - h + 1) >> 1;  // chunks h, h+2, ...
+      float *stg0 = reinterpret_cast<float *>(ring) + (warp * p.chunks_per_warp) * kStgFloats;
+      const int64_t wrow0 = tok0 + q * 32;  // first token of this warp's rows
+      int64_t wr = p.S - wrow0;              // valid rows of this warp (<= 0: none)
+      if (wr > p.TM - q * 32) wr = p.TM - q * 32;
+      const int wrows = wr > 32 ? 32 : int(wr);
+
+      // pass 1: logits (+ bias) into the shared tiles; top-2 candidates
+      float b1 = -INFINITY, b2 = -INFINITY;
+      int i1 = -1, i2 = -1;
+      for (int ci = 0; ci < my_chunks; ++ci) {
+        const int c = h + 2 * ci;
+        float *stg = stg0 + ci * kStgFloats;
+        uint32_t raw[32];
+        ptx::tmem_ld32(trow + uint32_t(c * 32), raw);
+        ptx::tmem_ld_wait();
+  #pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const int e = c * 32 + t;
+          if (e < E) {
+            const float v = __uint_as_float(raw[t]) + (brow ? brow[e] : ctl.bias[e]);
+            if (i1 < 0 || v > b1) {
+              b2 = b1;
+              i2 = i1;
+              b1 = v;
+              i1 = e;
+            } else if (i2 < 0 || v > b2) {
+              b2 = v;
+              i2 = e;
+            }
+            stg[lane * 33 + t] = v;
+          }
+        }
+        if (p.logits) {  // coalesced rows of the logits
+          __syncwarp();
+          const int e = c * 32 + lane;
+          for (int rr = 0; rr < wrows; ++rr)
+            if (e < E) p.logits[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
+        }
+      }
+      ptx::tc_fence_before();
+      ctl.cand_v[h][r][0] = b1;
+      ctl.cand_v[h][r][1] = b2;
+      ctl.cand_i[h][r][0] = i1;
+      ctl.cand_i[h][r][1] = i2;
+      block_sync();
+      // the row's top-2 over both halves: ranked by value, ties to the lower
+      // expert index (each half's candidates come in that order already)
+      {
+        const float ov1 = ctl.cand_v[h ^ 1][r][0], ov2 = ctl.cand_v[h ^ 1][r][1];
+        const int oi1 = ctl.cand_i[h ^ 1][r][0], oi2 = ctl.cand_i[h ^ 1][r][1];
+        auto before = [](float av, int ai, float bv, int bi) {
+          return ai >= 0 && (bi < 0 || av > bv || (av == bv && ai < bi));
+        };
+        if (before(ov1, oi1, b1, i1)) {
+          if (before(b1, i1, ov2, oi2)) {
+            b2 = b1;
+            i2 = i1;
+          } else {
+            b2 = ov2;
+            i2 = oi2;
+          }
+          b1 = ov1;
+          i1 = oi1;
+        } else if (before(ov1, oi1, b2, i2)) {
+          b2 = ov1;
+          i2 = oi1;
+        }
+      }
+      const float m = b1;  // the top-1 logit is the softmax shift
+      // pass 2: exp((l - m) / T) in place; this half's sum
+      float z = 0.0f;
+      for (int ci = 0; ci < my_chunks; ++ci) {
+        const int c = h + 2 * ci;
+        float *stg = stg0 + ci * kStgFloats;
+  #pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          if (c * 32 + t < E) {
+            const float ev = expf((stg[lane * 33 + t] - m) * p.inv_temp);
+            stg[lane * 33 + t] = ev;
+            z += ev;
+          }
+        }
+      }
+      ctl.zpart[h][r] = z;
+      block_sync();
+      const float inv_z = 1.0f / (ctl.zpart[0][r] + ctl.zpart[1][r]);
+      // pass 3: probabilities (0 past the batch), column sums over the tile's
+      // rows in a fixed order, the optional probability rows
+      for (int ci = 0; ci < my_chunks; ++ci) {
+        const int c = h + 2 * ci;
+        float *stg = stg0 + ci * kStgFloats;
+  #pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (c * 32 + t < E) stg[lane * 33 + t] = valid ? stg[lane * 33 + t] * inv_z : 0.0f;
+        __syncwarp();
+        const int e = c * 32 + lane;
+        float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows rr = 4 i + u, fixed order
+  #pragma unroll
+        for (int rr = 0; rr < 32; rr += 4) {
+  #pragma unroll
+          for (int u = 0; u < 4; ++u) cs[u] += stg[(rr + u) * 33 + lane];
+        }
+        if (e < E) ctl.psum_w[q][e] = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+        if (p.probs)
+          for (int rr = 0; rr < wrows; ++rr)
+            if (e < E) p.probs[(wrow0 + rr) * E + e] = stg[rr * 33 + lane];
+        __syncwarp();
+      }
+      if (h == 0) {
+        if (valid) {
+          p.idx[s * k] = i1;
+          if (k == 1) {
+            p.w[s] = inv_z;  // exp(l1 - max) = 1
+          } else {
+            const float x2 = expf((b2 - m) * p.inv_temp);
+            const float den = 1.0f + x2;
+            p.w[s * 2] = 1.0f / den;
+            p.w[s * 2 + 1] = x2 / den;
+            p.idx[s * 2 + 1] = i2;
+          }
+        }
+        ctl.choice[0][r] = valid ? i1 : -1;
+        ctl.choice[1][r] = (valid && k == 2) ? i2 : -1;
+      }
+    }
+    block_sync();
+
+    if (warp >= 4) {
+      // the tile's count and each token's rank per (j, e), in token order:
+      // within a warp by __match_any_sync, across the 4 warps by their counts'
+      // prefix; both choices at once, the counts in the ring (idle now)
+      const int q = warp & 3;
+      const int r = q * 32 + lane;
+      const int et = tid - 128;  // 0..127 over warps 4..7
+      int32_t *wc = reinterpret_cast<int32_t *>(ring);  // [k][4][E]
+      for (int i = et; i < k * 4 * E; i += 128) wc[i] = 0;
+      epi_sync();
+      int ej[2], rk[2];
+  #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        ej[j] = j < k ? ctl.choice[j][r] : -1;
+        const unsigned peers = __match_any_sync(kFullMask, ej[j]);
+        rk[j] = __popc(peers & lanemask_lt());
+        if (ej[j] >= 0 && rk[j] == 0) wc[(j * 4 + q) * E + ej[j]] = __popc(peers);
+      }
+      epi_sync();
+      for (int i = et; i < k * E; i += 128) {
+        const int j = i / E, ee = i - j * E;
+        int run = 0;
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int cnum = wc[(j * 4 + w4) * E + ee];
+          wc[(j * 4 + w4) * E + ee] = run;
+          run += cnum;
+        }
+        ctl.cnt[j][ee] = run;
+      }
+      epi_sync();
+  #pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (j < k) ctl.rank[j][r] = ej[j] >= 0 ? wc[(j * 4 + q) * E + ej[j]] + rk[j] : 0;
+    } else {
+      // publish the tile's probability sums (padding entries 0)
+      for (int e = tid; e < p.psum_pitch; e += 128)
+        p.psum[int64_t(tile) * p.psum_pitch + e] =
+            e < E ? ((ctl.psum_w[0][e] + ctl.psum_w[1][e]) + ctl.psum_w[2][e]) + ctl.psum_w[3][e]
+                  : 0.0f;
+    }
+    block_sync();
+    // publish the tile's counts (padding entries 0)
+    for (int i = tid; i < p.hist_pitch; i += kGrThreads)
+      p.hist[int64_t(tile) * p.hist_pitch + i] = i < k * E ? ctl.cnt[i / E][i % E] : 0;
+
+    ptx::tc_fence_before();
+    block_sync();
+    if (warp == 1) {
+      ptx::tc_fence_after();
+      ptx::tmem_dealloc(tmem, p.tmem_cols);
+    }
   }
 
   // ------------------------------------------------------- grid barrier
   if (tid == 0) {
-    const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles), lim);
+    const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles) + 1u, lim);
     if (!ok) record_error(p.err, kErrGateBarrier | uint32_t(tile & 0xffffff));
     ctl.barrier_ok = ok ? 1 : 0;
   }
   block_sync();
   // Without the barrier some tiles' counts may be missing: every choice of
-  // this tile is then dropped and tile 0 reports empty experts.
+  // this tile is then dropped and the last CTA reports empty experts.
   const bool okb = ctl.barrier_ok != 0;
 
   // ------------------------------------------------------------ phase B
@@ -576,7 +582,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       // offsets never pass the rows the buffers hold (true by construction
       // when every tile's counts arrived)
       ctl.offs[e] = run < p.rows_alloc ? run : int(p.rows_alloc);
-      if (tile == 0) {
+      if (tile == p.ntiles) {
         p.routed[e] = rt;
         p.kept[e] = kp;
         p.offsets[e] = ctl.offs[e];
@@ -585,7 +591,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     }
     if (lane == 31) {
       ctl.offs[E] = incl < p.rows_alloc ? incl : int(p.rows_alloc);
-      if (tile == 0) p.offsets[E] = ctl.offs[E];
+      if (tile == p.ntiles) p.offsets[E] = ctl.offs[E];
     }
   }
   block_sync();
@@ -603,8 +609,8 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     p.slot[s * k + j] = pos;
     if (pos >= 0) p.row_src[ctl.offs[e] + pos] = int32_t(s * k + j);
   }
-  // l_aux (tile 0): probability sums over all tiles, as exact fixed-point
-  if (tile == 0) {
+  // l_aux (the last CTA): probability sums over all tiles, as exact fixed-point
+  if (tile == p.ntiles) {
     const int nv = p.psum_pitch >> 2;
     const int RG = max(1, kGrThreads / nv);
     const int v = tid % nv, g = tid / nv;
@@ -621,10 +627,10 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-          a[0] += __float2ll_rn(f[u].x * 1073741824.0f);
-          a[1] += __float2ll_rn(f[u].y * 1073741824.0f);
-          a[2] += __float2ll_rn(f[u].z * 1073741824.0f);
-          a[3] += __float2ll_rn(f[u].w * 1073741824.0f);
+          a[0] += fix30_tile(f[u].x);
+          a[1] += fix30_tile(f[u].y);
+          a[2] += fix30_tile(f[u].z);
+          a[3] += fix30_tile(f[u].w);
         }
       }
     }
@@ -686,8 +692,10 @@ cudaError_t set_gate_wait_limit(uint64_t ns) {
 
 cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   if (a.S <= 0) return cudaErrorNotSupported;
-  const int nsm = num_sms();
-  int64_t tm = (a.S + nsm - 1) / nsm;
+  // one tile per SM but one: that SM runs the CTA that publishes the counts
+  const int ntile_max = num_sms() - 1;
+  if (ntile_max < 1) return cudaErrorNotSupported;
+  int64_t tm = (a.S + ntile_max - 1) / ntile_max;
   tm = (tm + 7) & ~int64_t(7);
   if (tm < 16) tm = 16;
   if (tm > kGrMaxTile) return cudaErrorNotSupported;  // more tokens than one wave of tiles
@@ -699,15 +707,21 @@ cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   uint32_t cols = 32;
   while (int(cols) < p.E_pad) cols <<= 1;
   p.tmem_cols = cols;
-  p.nbox = MOE_GATE_BOXES;
-  p.nk64 = (a.d + 63) / 64;
-  p.nk = (p.nk64 + p.nbox - 1) / p.nbox;
-  p.stage_bytes = uint32_t(p.nbox) * (kXBoxBytes + uint32_t(p.E_pad) * 128);
+  // ring stages of nbox 64-wide K boxes: the widest boxes (each tile row
+  // read in longer runs) that still leave two stages in flight
   constexpr size_t kSmemLimit = 232448;
   const size_t fixed = 1024 + sizeof(GrCtl);
-  int nst = int((kSmemLimit - fixed) / p.stage_bytes);
-  if (nst > kGrMaxStages) nst = kGrMaxStages;
-  if (nst > p.nk) nst = p.nk;
+  p.nk64 = (a.d + 63) / 64;
+  int nst = 0;
+  for (int nb = kGrMaxBoxes; nb >= 1; nb >>= 1) {
+    p.nbox = nb;
+    p.nk = (p.nk64 + nb - 1) / nb;
+    p.stage_bytes = uint32_t(nb) * (kXBoxBytes + uint32_t(p.E_pad) * 128);
+    nst = int((kSmemLimit - fixed) / p.stage_bytes);
+    if (nst > kGrMaxStages) nst = kGrMaxStages;
+    if (nst > p.nk) nst = p.nk;
+    if (nst >= 2 || (nb == 1 && nst >= 1)) break;
+  }
   if (nst < 1) return cudaErrorNotSupported;
   p.nstages = nst;
   p.hist_pitch = (a.k * a.E + 3) & ~3;
@@ -758,7 +772,7 @@ cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(unsigned(p.ntiles));
+  lc.gridDim = dim3(unsigned(p.ntiles) + 1u);  // + the CTA that publishes counts and l_aux
   lc.blockDim = dim3(kGrThreads);
   lc.dynamicSmemBytes = smem;
   lc.stream = st;

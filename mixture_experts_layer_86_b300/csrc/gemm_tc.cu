@@ -40,7 +40,6 @@
 
 #include "common.cuh"
 #include "kernels.h"
-#include "rng.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -78,9 +77,33 @@ struct TileCoord {
   int ntok;       // valid tokens of this tile (1..kTok)
 };
 
+// Tile order: group by group, token tile by token tile, the nf feature
+// tiles of each token tile in turn.  Tiles go to the persistent CTAs
+// round-robin, so the pairs working at one time share the group's weights
+// and token rows in L2 (a group's partial last token tile comes right after
+// its whole ones, while its weights are still there).
+template <typename Ctl>
+__device__ __forceinline__ void tile_plan(Ctl &c, int G, int nf, const int32_t *offsets,
+                                          int64_t dense_rows) {
+  // without offsets the rows form one group of dense_rows rows
+  for (int g = 0; g <= G; ++g)
+    c.row_start[g] = offsets ? offsets[g] : (g == 0 ? 0 : int(dense_rows));
+  int run = 0;
+  for (int g = 0; g < G; ++g) {
+    c.tile_start[g] = run;
+    run += ((c.row_start[g + 1] - c.row_start[g] + kTok - 1) / kTok) * nf;
+  }
+  c.tile_start[G] = run;
+}
+
+template <typename Ctl>
+__device__ __forceinline__ int tile_total(const Ctl &c, int G) {
+  return c.tile_start[G];
+}
+
 template <typename Ctl>
 __device__ __forceinline__ TileCoord tile_coord(const Ctl &c, int G, int nf, int t) {
-  int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t
+  int lo = 0, hi = G - 1;  // last g with tile_start[g] <= t (groups without tiles skipped)
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (c.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
@@ -151,15 +174,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
-    // without offsets the rows form one group of dense_rows rows
-    for (int g = 0; g <= G; ++g)
-      ctl.row_start[g] = offsets ? offsets[g] : (g == 0 ? 0 : int(dense_rows));
-    int run = 0;
-    for (int g = 0; g < G; ++g) {
-      ctl.tile_start[g] = run;
-      run += ((ctl.row_start[g + 1] - ctl.row_start[g] + kTok - 1) / kTok) * nf;
-    }
-    ctl.tile_start[G] = run;
+    tile_plan(ctl, G, nf, offsets, dense_rows);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -175,7 +190,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
   block_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
-  const int total = ctl.tile_start[G];
+  const int total = tile_total(ctl, G);
   volatile int *abort = &ctl.abort;
 
   if (warp == 0) {
@@ -433,7 +448,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                     const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err,
                     const __nv_bfloat16 *__restrict__ xg, const int32_t *__restrict__ row_src,
-                    int kch, int b_wrap, const TcRouterEpi rt) {
+                    int kch, int b_wrap, float *__restrict__ c_f32) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -463,15 +478,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort = 0;
-    // without offsets the rows form one group of dense_rows rows
-    for (int g = 0; g <= G; ++g)
-      ctl.row_start[g] = offsets ? offsets[g] : (g == 0 ? 0 : int(dense_rows));
-    int run = 0;
-    for (int g = 0; g < G; ++g) {
-      ctl.tile_start[g] = run;
-      run += ((ctl.row_start[g + 1] - ctl.row_start[g] + kTok - 1) / kTok) * nf;
-    }
-    ctl.tile_start[G] = run;
+    tile_plan(ctl, G, nf, offsets, dense_rows);
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
@@ -488,7 +495,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
   ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
-  const int total = ctl.tile_start[G];
+  const int total = tile_total(ctl, G);
   volatile int *abort = &ctl.abort;
 
   if (warp == 0) {
@@ -714,55 +721,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]) + bv;
-        if (kWMN && rt.src) {
-          // router form: x = acc * f(s, n) + the experts' rows of token s
-          const auto *src = static_cast<const __nv_bfloat16 *>(rt.src);
-          int r0 = -1, r1 = -1;  // lane t: the rows of this chunk's token t
-          if (lane < ntk) {
-            r0 = rt.rows[(trow0 + lane) * rt.k];
-            if (rt.k == 2) r1 = rt.rows[(trow0 + lane) * 2 + 1];
-          }
-          if (rt.jitter) {
-            const rng::Key key = rng::make_key(rt.noise.seed, rt.noise.offset);
-            const float eps = rt.noise.jitter_eps > 0.0f ? rt.noise.jitter_eps : 0.01f;
-            // one token per pass; x rotates by one so that only x[0] is
-            // indexed (a rolled loop with static register indices)
-#pragma unroll 1
-            for (int i = 0; i < 32; ++i) {
-              float fac = 1.0f;
-              if (i < ntk) {
-                const uint4 w4 = rng::block(key, rng::kPurposeJitter, uint32_t(trow0 + i),
-                                            uint32_t(f >> 2));
-                fac = rng::jitter(rng::uniform(rng::word(w4, f & 3)), eps);
-              }
-              const float t = x[0] * fac;
-#pragma unroll
-              for (int j = 0; j < 31; ++j) x[j] = x[j + 1];
-              x[31] = t;
-            }
-          }
-          // per choice: the chunk's 32 row segments (32 features, 64 B each)
-          // gathered through the staging tile, 4 16-byte loads in flight per
-          // lane, then added column by column
-#pragma unroll 1
-          for (int j = 0; j < rt.k; ++j) {
-            const int rj = j == 0 ? r0 : r1;
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-              const int tr = s4 * 8 + pr, fc = f0 + pp * 8;
-              const int row = __shfl_sync(kFullMask, rj, tr);
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (row >= 0 && fc < N)
-                v = *reinterpret_cast<const uint4 *>(src + int64_t(row) * N + fc);
-              *reinterpret_cast<uint4 *>(stg + tr * 64 + pp * 16) = v;
-            }
-            __syncwarp();
+        if (kWMN && c_f32) {
+          // router form: the fp32 accumulator, each store one 128-byte
+          // segment of a token row (lane = feature)
+          if (f < N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              x[i] += __bfloat162float(
-                  *reinterpret_cast<const __nv_bfloat16 *>(stg + i * 64 + lane * 2));
-            __syncwarp();
+              if (i < ntk) c_f32[(trow0 + i) * N + f] = x[i];
           }
+          continue;
         }
         if (grad_src) {
 #pragma unroll
@@ -1357,10 +1324,10 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
           break;
         }
         const int valid = rows - kb * kWpBK;  // rows of this stage inside the group
-        if (valid < kWpBK) {
-          // rows [max(valid, 64 zh + zr0), 64 zh + zr0 + 32) of both operands
-          const int vr = max(0, min(32, valid - (64 * zh + zr0)));
-          const int nbytes = (32 - vr) * 128;
+        // rows [max(valid, 64 zh + zr0), 64 zh + zr0 + 32) of both operands
+        const int vr = max(0, min(32, valid - (64 * zh + zr0)));
+        const int nbytes = (32 - vr) * 128;   // 0: nothing of this warp's to zero
+        if (nbytes > 0) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -1389,9 +1356,16 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             acc[3] += __uint_as_float(v.y & 0xffff0000u);
           }
         }
-        ptx::fence_proxy_async_smem();  // this warp's zeroes are visible to the MMA's reads
+        // this warp's zeroes (if any) are visible to the MMA's reads; the
+        // even CTA's warps arrive on their own barrier directly
+        if (nbytes > 0) ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_remote(ready_leader + uint32_t(st) * 8u);
+        if (lane == 0) {
+          if (rank == 0)
+            ptx::mbar_arrive(ptx::smem_addr(&ctl.ready[st]));
+          else
+            ptx::mbar_arrive_remote(ready_leader + uint32_t(st) * 8u);
+        }
       }
       if (sum && ok) {
         // the 4 row groups' sums, in row-group order (lanes q, q+8, q+16, q+24)
@@ -1698,9 +1672,9 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
                               static_cast<__nv_bfloat16 *>(g.pre),
                               static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err,
                               static_cast<const __nv_bfloat16 *>(g.A), g.row_src, g.k_choices,
-                              g.b_wrap, g.rt);
+                              g.b_wrap, g.c_f32);
   }
-  if (g.row_src || g.b_wrap || g.rt.src)
+  if (g.row_src || g.b_wrap || g.c_f32)
     return cudaErrorNotSupported;  // the gather and router forms need CTA pairs
   static PerDevice<int> smem_raised[2];
   const int which = g.b_kmajor ? 0 : 1;

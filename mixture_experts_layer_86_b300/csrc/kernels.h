@@ -187,18 +187,10 @@ cudaError_t launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
 // and row r of the grouped operand is token row_src[r] / k_choices of it
 // (the dispatch copy fused into the GEMM); C, pre and the groups keep the
 // expert-major row order.  Needs b_kmajor and CTA pairs.
-// Router form of the input gradient (rt.src set; one group, !b_kmajor, CTA
-// pairs): row k of B is row k mod b_wrap of a [b_rows, N] matrix (rows past
-// b_rows read as zero), and the epilogue stores, per token row s,
-//   C[s, n] = acc * f(s, n) + sum_j src[rows[s, j], n]
-// over the kept choices (rows[s, j] >= 0), f the jitter factor (1 without).
-struct TcRouterEpi {
-  const void *src;            // [rows, N] bf16: the experts' input-gradient rows
-  const int32_t *rows;        // [S, k]: row of each choice in src, -1 when dropped
-  int k;
-  int jitter;                 // nonzero: multiply acc by the jitter factor
-  RouteNoise noise;
-};
+// Router form (c_f32 set; one group, !b_kmajor, CTA pairs): row k of B is
+// row k mod b_wrap of a [b_rows, N] matrix (rows past b_rows read as zero)
+// and the epilogue stores the fp32 accumulator to c_f32 [rows, N] (no bias,
+// activation or bf16 output).
 struct TcGemm {
   const void *A; int64_t rows_alloc;   // rows of the A/C allocations
   const void *B; bool b_kmajor;
@@ -213,7 +205,7 @@ struct TcGemm {
   const int32_t *row_src;  // gather form: [rows] s*k+j of each row, else null
   int k_choices;
   int b_wrap, b_rows;      // router form: K rows of B repeat every b_wrap rows (0: off)
-  TcRouterEpi rt;
+  float *c_f32;
 };
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 
@@ -295,11 +287,13 @@ size_t gate_wgrad_tc_partial_bytes(int64_t S, int E, int d);
 cudaError_t launch_gate_wgrad_tc(const void *x, const void *dl2, int64_t S, int d, int E,
                                  float *partial, void *dw_gate, unsigned int *err,
                                  cudaStream_t st);
-// dX = [hi | lo] [W_g; W_g] (* jitter factor) + sum_j dx_disp[row(s, j)]: the
-// CTA-pair GEMM with the router epilogue.
+// dX = r * f + sum_j dx_disp[rows[s, j]] with the router term
+// r = [hi | lo] [W_g; W_g] (fp32 [S, d], the CTA-pair GEMM's router form)
+// and f the jitter factor (1 without jitter).
 cudaError_t launch_dx_router_tc(const void *dl2, const void *w_gate, const void *dx_disp,
-                                int64_t S, int d, int E, int k, const int32_t *rows, void *dx,
-                                const RouteNoise *jitter, unsigned int *err, cudaStream_t st);
+                                int64_t S, int d, int E, int k, const int32_t *rows,
+                                float *rterm, void *dx, const RouteNoise *jitter,
+                                unsigned int *err, cudaStream_t st);
 // dW_g = dlogits^T x: token-split fp32 partial sums, then a fixed-order sum.
 int64_t gate_wgrad_splits(int64_t S);
 size_t gate_wgrad_partial_bytes(int64_t S, int E, int d);

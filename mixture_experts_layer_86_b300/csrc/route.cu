@@ -268,7 +268,7 @@ route_scan_kernel(int64_t nblk, int64_t S, int E, int k, int64_t cap, int aux_ty
     const int64_t b1 = act ? min(nblk, b0 + per) : 0;
     long long ps = 0;
 #pragma unroll 4
-    for (int64_t b = b0; b < b1; ++b) ps += __float2ll_rn(psum[b * E + e] * 1073741824.0f);
+    for (int64_t b = b0; b < b1; ++b) ps += fix30_tile(psum[b * E + e]);
     if (act) s_pgrp[g * E + e] = ps;
     block_sync();
     if (threadIdx.x < E) {
