@@ -118,6 +118,7 @@ struct BwdWs {
   float *aux_coef;
   void *xj;       // the jittered router input (MOE_NOISE_JITTER only)
   int32_t *rows;  // [S, k] row of each choice in the expert-major buffers, -1 when dropped
+  void *maps;     // per-expert tensor maps of the two weight-gradient GEMMs (bf16)
 };
 
 // The router's backward: fp32 layers keep dlogits [S,E] fp32 and CUDA-core
@@ -130,7 +131,7 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const bool tc = c->dtype == MOE_BF16;
   // slot 0 (dO) also holds the router term r [S, d] fp32 of bf16 layers,
   // which is formed after the last use of dO
-  const size_t sz[9] = {align256(std::max(size_t(R) * c->hidden_size * eb,
+  const size_t sz[10] = {align256(std::max(size_t(R) * c->hidden_size * eb,
                                           tc ? size_t(S) * c->hidden_size * 4 : size_t(0))),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
@@ -143,7 +144,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
                                                                c->hidden_size)),
                         align256(size_t(c->num_experts) * 4),
                         jitter_bytes(c),
-                        align256(size_t(S) * c->k * 4)};
+                        align256(size_t(S) * c->k * 4),
+                        tc ? align256(size_t(4) * c->num_experts * kTensorMapBytes) : 0};
   if (w) {
     char *p = static_cast<char *>(base);
     w->d_out = p; p += sz[0];
@@ -154,7 +156,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->gate_partial = reinterpret_cast<float *>(p); p += sz[5];
     w->aux_coef = reinterpret_cast<float *>(p); p += sz[6];
     w->xj = sz[7] ? p : nullptr; p += sz[7];
-    w->rows = reinterpret_cast<int32_t *>(p);
+    w->rows = reinterpret_cast<int32_t *>(p); p += sz[8];
+    w->maps = sz[9] ? p : nullptr;
   }
   size_t total = 0;
   for (size_t v : sz) total += v;
@@ -592,6 +595,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     g.A = w.d_out; g.B = sv->h; g.rows_alloc = R > 0 ? R : 1; g.C = dw2;
     g.M = d; g.N = f; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
     g.colsum = db2;
+    g.group_maps = w.maps;
     cudaError_t e = launch_tc_wgrad(g, st);
     db2_done = e == cudaSuccess;
     if (e == cudaErrorNotSupported) {
@@ -636,6 +640,9 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     g.A = w.dh_pre; g.B = sv->x_disp; g.rows_alloc = R > 0 ? R : 1; g.C = dw1;
     g.M = f; g.N = d; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
     g.colsum = db1;
+    // its own maps: the dW2 launch may still be reading the first half
+    g.group_maps = w.maps ? static_cast<char *>(w.maps) + 2 * size_t(E) * kTensorMapBytes
+                          : nullptr;
     cudaError_t e = launch_tc_wgrad(g, st);
     db1_done = e == cudaSuccess;
     if (e == cudaErrorNotSupported) {

@@ -1105,17 +1105,21 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // stage: 64 KB per CTA per stage instead of the 96 KB that a single-CTA
 // 128 x 256 tile needs for the same work.
 // A stage takes one of two paths:
-//   direct  (a K block wholly inside the group, no column sums): both CTAs'
-//           TMA copies complete on the even CTA's `full` barrier, which the
-//           MMA waits on -- the forward pair GEMM's path;
-//   relayed (the group's last, partial K block -- its rows past the group
-//           hold the next group's rows or unwritten memory and must read as
-//           zero -- or any K block of a first-N tile, whose A columns also
-//           give the bias gradient db_g = sum over rows of A): each CTA's
-//           copies complete on its own `tail` barrier; its 4 relay warps
-//           zero the rows past the group (each a quarter of the rows), add
-//           A's valid rows column by column (each a quarter of the
-//           columns), fence the stage for the tensor cores and arrive on
+//   direct  (no column sums): both CTAs' TMA copies complete on the even
+//           CTA's `full` barrier, which the MMA waits on -- the forward pair
+//           GEMM's path.  A group's last, partial K block is direct too when
+//           the launch has per-group tensor maps (the operands' maps cut to
+//           the group's end row, written on the device by
+//           wgrad_group_maps_kernel): TMA reads the rows past the group as
+//           zeros, where they would otherwise hold the next group's rows or
+//           unwritten memory;
+//   relayed (any K block of a first-N tile, whose A columns also give the
+//           bias gradient db_g = sum over rows of A, and without per-group
+//           maps the partial last block): each CTA's copies complete on its
+//           own `tail` barrier; its 4 relay warps zero the rows past the
+//           group unless TMA did (each a quarter of the rows), add A's valid
+//           rows column by column (each a quarter of the columns), fence the
+//           stage for the tensor cores if they wrote to it, and arrive on
 //           the even CTA's `ready` barrier, which the MMA waits on.
 // Both CTAs walk the same tiles and K blocks, so every role agrees on each
 // stage's path; the phase of each barrier kind is tracked per stage.
@@ -1148,9 +1152,39 @@ constexpr uint32_t kWpStgBytes = 32 * 64;
 constexpr size_t kWpSmemBytes =
     1024 + kWpStages * 2 * kWpOpBytes + kWpEpiWarps * kWpStgBytes + sizeof(WpCtl);
 
-// whether K block kb of a group with `rows` rows goes through the relay
-__device__ __forceinline__ bool wp_relayed(int rows, int kb, bool sum) {
-  return sum || rows - kb * kWpBK < kWpBK;
+// whether K block kb of a group with `rows` rows goes through the relay:
+// a block of a bias-sum tile, or the group's partial last block when there
+// are no per-group tensor maps to zero-fill the rows past the group
+__device__ __forceinline__ bool wp_relayed(int rows, int kb, bool sum, bool zero_fill) {
+  return sum || (!zero_fill && rows - kb * kWpBK < kWpBK);
+}
+
+// Per-group tensor maps of the two operands: the launch's maps with the
+// outer extent cut to the group's end row, so that TMA fills the rows past
+// the group with zeros.  One warp per group; maps[2g] is A's, maps[2g+1] B's.
+__global__ void __launch_bounds__(256)
+wgrad_group_maps_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const int32_t *__restrict__ offsets, int G, CUtensorMap *maps) {
+  griddep_begin();
+  __shared__ __align__(128) uint4 sm[8][2][8];  // per warp: A's and B's 128 bytes
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * 8 + warp;
+  if (g >= G) return;  // the whole warp
+  if (lane < 16) {
+    const CUtensorMap *src = lane < 8 ? &tmA : &tmB;
+    sm[warp][lane >> 3][lane & 7] = reinterpret_cast<const uint4 *>(src)[lane & 7];
+  }
+  __syncwarp();
+  if (lane == 0) {
+    const int end = offsets[g + 1];
+    const uint32_t extent = uint32_t(end > 0 ? end : 1);
+    ptx::tensormap_set_dim1(ptx::smem_addr(&sm[warp][0][0]), extent);
+    ptx::tensormap_set_dim1(ptx::smem_addr(&sm[warp][1][0]), extent);
+  }
+  __syncwarp();
+  ptx::tensormap_publish(&maps[2 * g], ptx::smem_addr(&sm[warp][0][0]));
+  ptx::tensormap_publish(&maps[2 * g + 1], ptx::smem_addr(&sm[warp][1][0]));
 }
 
 // Stage layout of one operand half: [k half 0: cols 0-63, cols 64-127]
@@ -1161,7 +1195,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
                      const int32_t *__restrict__ offsets, int G, int M, int N,
                      __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ colsum,
-                     unsigned int *err) {
+                     unsigned int *err, const CUtensorMap *__restrict__ gmaps) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1176,6 +1210,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   const int mt = (M + 255) / 256, nt = (N + 255) / 256;
   const int total = G * mt * nt;
   const bool with_sum = colsum != nullptr;
+  const bool zero_fill = gmaps != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWpStages; ++s) {
@@ -1232,7 +1267,17 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             break;
           }
           const int row = r0 + kb * kWpBK;
-          if (wp_relayed(rows, kb, sum)) {
+          // the group's partial last block through the group's own maps
+          // (rows past the group read as zero), the others through the launch's
+          const bool part = rows - kb * kWpBK < kWpBK;
+          const CUtensorMap *ma = &tmA, *mb = &tmB;
+          if (zero_fill && part) {
+            ma = gmaps + 2 * g;
+            mb = ma + 1;
+            ptx::tensormap_acquire(ma);
+            ptx::tensormap_acquire(mb);
+          }
+          if (wp_relayed(rows, kb, sum, zero_fill)) {
             const uint32_t tb = ptx::smem_addr(&ctl.tail[stage]);
             ptx::mbar_arrive_expect_tx(tb, 2 * kWpOpBytes);
 #pragma unroll
@@ -1240,8 +1285,8 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
-                ptx::tma_load_2d(ptx::smem_addr(sA + off), &tmA, tb, acol + j * 64, row + h * 64);
-                ptx::tma_load_2d(ptx::smem_addr(sB + off), &tmB, tb, bcol + j * 64, row + h * 64);
+                ptx::tma_load_2d(ptx::smem_addr(sA + off), ma, tb, acol + j * 64, row + h * 64);
+                ptx::tma_load_2d(ptx::smem_addr(sB + off), mb, tb, bcol + j * 64, row + h * 64);
               }
             tail_armed |= 1u << stage;
             tail_ph ^= 1u << stage;
@@ -1254,9 +1299,9 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const uint32_t off = stage * kWpOpBytes + (h * 2 + j) * kWpBoxBytes;
-                ptx::tma_load_2d_pair(ptx::smem_addr(sA + off), &tmA, fb, acol + j * 64,
+                ptx::tma_load_2d_pair(ptx::smem_addr(sA + off), ma, fb, acol + j * 64,
                                       row + h * 64);
-                ptx::tma_load_2d_pair(ptx::smem_addr(sB + off), &tmB, fb, bcol + j * 64,
+                ptx::tma_load_2d_pair(ptx::smem_addr(sB + off), mb, fb, bcol + j * 64,
                                       row + h * 64);
               }
           }
@@ -1308,7 +1353,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int kb = 0; kb < nk; ++kb) {
         const int st = stage;
         if (++stage == kWpStages) stage = 0;
-        if (!wp_relayed(rows, kb, sum)) continue;
+        if (!wp_relayed(rows, kb, sum, zero_fill)) continue;
         bool got = true;
         if (lane == 0)
           got = ptx::mbar_wait(ptx::smem_addr(&ctl.tail[st]), (tail_ph >> st) & 1u, abort,
@@ -1326,7 +1371,8 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         const int valid = rows - kb * kWpBK;  // rows of this stage inside the group
         // rows [max(valid, 64 zh + zr0), 64 zh + zr0 + 32) of both operands
         const int vr = max(0, min(32, valid - (64 * zh + zr0)));
-        const int nbytes = (32 - vr) * 128;   // 0: nothing of this warp's to zero
+        // 0: nothing of this warp's to zero (or TMA filled those rows with zeros)
+        const int nbytes = zero_fill ? 0 : (32 - vr) * 128;
         if (nbytes > 0) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -1411,7 +1457,7 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * 256);
         for (int kb = 0; kb < nk; ++kb) {
-          const bool relayed = wp_relayed(rows, kb, sum);
+          const bool relayed = wp_relayed(rows, kb, sum, zero_fill);
           const uint32_t bar =
               ptx::smem_addr(relayed ? &ctl.ready[stage] : &ctl.full[stage]);
           const uint32_t par = ((relayed ? ready_ph : full_ph) >> stage) & 1u;
@@ -1591,9 +1637,16 @@ cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int tiles = g.G * ((g.M + 255) / 256) * ((g.N + 255) / 256);
     lc.gridDim = dim3(2 * (tiles < npairs ? tiles : npairs));
+    CUtensorMap *gmaps = static_cast<CUtensorMap *>(g.group_maps);
+    if (gmaps) {
+      const cudaError_t em = launch_k(wgrad_group_maps_kernel, unsigned((g.G + 7) / 8), 256, 0,
+                                      st, ta, tb, g.offsets, g.G, gmaps);
+      if (em != cudaSuccess) return em;
+    }
     return cudaLaunchKernelEx(&lc, tc_wgrad_pair_kernel, ta, tb, g.offsets, g.G, g.M, g.N,
                               static_cast<__nv_bfloat16 *>(g.C),
-                              static_cast<__nv_bfloat16 *>(g.colsum), g.err);
+                              static_cast<__nv_bfloat16 *>(g.colsum), g.err,
+                              static_cast<const CUtensorMap *>(gmaps));
   }
   if (g.colsum) return cudaErrorNotSupported;  // the single-CTA kernel has no column sums
   if (!g.offsets && g.chunk_rows <= 0) return cudaErrorInvalidValue;

@@ -217,7 +217,11 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 // Cf (fp32, nullable) replaces C; offsets == null makes group g the rows
 // [g * chunk_rows, min((g + 1) * chunk_rows, rows_alloc)) (a split of one
 // long reduction into partial sums, each written to its own C_g); single
-// takes the one-CTA kernel.
+// takes the one-CTA kernel.  group_maps (nullable, CTA pairs): device
+// memory for 2 * G tensor maps (128 bytes each, 128-byte aligned) that a
+// setup launch fills with the operands' maps cut to each group's end row,
+// so the groups' partial last K blocks load with zeros past the group.
+constexpr size_t kTensorMapBytes = 128;
 struct TcWgrad {
   const void *A; const void *B; int64_t rows_alloc;
   void *C;
@@ -228,6 +232,7 @@ struct TcWgrad {
   float *Cf;
   int chunk_rows;
   bool single;
+  void *group_maps;
 };
 cudaError_t launch_tc_wgrad(const TcWgrad &g, cudaStream_t st);
 

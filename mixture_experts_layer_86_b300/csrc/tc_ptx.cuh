@@ -77,6 +77,30 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Tensor maps edited on the device (one per group of a grouped GEMM): a copy
+// of a map in shared memory gets a new outer extent, then the warp copies it
+// to global memory with the release fence of the tensor-map proxy; a thread
+// that loads with it first runs the matching acquire fence.
+__device__ __forceinline__ void tensormap_set_dim1(uint32_t smem_map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(
+                   smem_map),
+               "r"(extent)
+               : "memory");
+}
+// all 32 lanes of the warp, the same operands
+__device__ __forceinline__ void tensormap_publish(void *gmem_map, uint32_t smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned "
+      "[%0], [%1], 128;" ::"l"(reinterpret_cast<uint64_t>(gmem_map)),
+      "r"(smem_map)
+      : "memory");
+}
+__device__ __forceinline__ void tensormap_acquire(const void *gmem_map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(gmem_map))
+               : "memory");
+}
+
 // ------------------------------------------------------------ cp.async
 // 16-byte copy global -> shared through L2 (not L1).  With src_bytes = 0
 // nothing is read and the 16 bytes are filled with zeros.  The copy is a
