@@ -119,6 +119,7 @@ struct BwdWs {
   void *xj;       // the jittered router input (MOE_NOISE_JITTER only)
   int32_t *rows;  // [S, k] row of each choice in the expert-major buffers, -1 when dropped
   void *maps;     // per-expert tensor maps of the two weight-gradient GEMMs (bf16)
+  float *colpart; // partial column sums of dh_pre from the data-gradient epilogue (bf16)
 };
 
 // The router's backward: fp32 layers keep dlogits [S,E] fp32 and CUDA-core
@@ -131,7 +132,7 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
   const bool tc = c->dtype == MOE_BF16;
   // slot 0 (dO) also holds the router term r [S, d] fp32 of bf16 layers,
   // which is formed after the last use of dO
-  const size_t sz[10] = {align256(std::max(size_t(R) * c->hidden_size * eb,
+  const size_t sz[11] = {align256(std::max(size_t(R) * c->hidden_size * eb,
                                           tc ? size_t(S) * c->hidden_size * 4 : size_t(0))),
                         align256(size_t(R) * c->ffn_size * eb),
                         align256(size_t(R) * c->hidden_size * eb),
@@ -145,7 +146,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
                         align256(size_t(c->num_experts) * 4),
                         jitter_bytes(c),
                         align256(size_t(S) * c->k * 4),
-                        tc ? align256(size_t(4) * c->num_experts * kTensorMapBytes) : 0};
+                        tc ? align256(size_t(4) * c->num_experts * kTensorMapBytes) : 0,
+                        tc ? align256(bias_grad_part_bytes(R, c->num_experts, c->ffn_size)) : 0};
   if (w) {
     char *p = static_cast<char *>(base);
     w->d_out = p; p += sz[0];
@@ -157,7 +159,8 @@ size_t bwd_ws_carve(const moe_config *c, void *base, BwdWs *w) {
     w->aux_coef = reinterpret_cast<float *>(p); p += sz[6];
     w->xj = sz[7] ? p : nullptr; p += sz[7];
     w->rows = reinterpret_cast<int32_t *>(p); p += sz[8];
-    w->maps = sz[9] ? p : nullptr;
+    w->maps = sz[9] ? p : nullptr; p += sz[9];
+    w->colpart = sz[10] ? reinterpret_cast<float *>(p) : nullptr;
   }
   size_t total = 0;
   for (size_t v : sz) total += v;
@@ -594,10 +597,12 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
     TcWgrad g{};
     g.A = w.d_out; g.B = sv->h; g.rows_alloc = R > 0 ? R : 1; g.C = dw2;
     g.M = d; g.N = f; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
-    g.colsum = db2;
+    // the bias gradient by a column-sum kernel: in the GEMM it would send
+    // the first-N tiles' stages through the relay warps
+    g.colsum = nullptr;
     g.group_maps = w.maps;
     cudaError_t e = launch_tc_wgrad(g, st);
-    db2_done = e == cudaSuccess;
+    db2_done = e == cudaSuccess && g.colsum != nullptr;
     if (e == cudaErrorNotSupported) {
       g.colsum = nullptr;
       e = launch_tc_wgrad(g, st);
@@ -621,6 +626,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
       g.A = w.d_out; g.rows_alloc = R; g.B = w2; g.b_kmajor = false; g.C = w.dh_pre;
       g.N = f; g.K = d; g.G = E; g.offsets = sv->expert_offsets; g.bias = nullptr; g.act = -1;
       g.pre = nullptr; g.grad_src = sv->h_pre; g.dact = cfg->act; g.err = device_error_ptr();
+      g.col_part = w.colpart;  // db1's partial sums, from the values it stores
       MOE_CUDA(launch_tc_gemm(g, st));
     } else {
       SimtGemm g{};
@@ -633,18 +639,23 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const void *w_gate
       MOE_CUDA(launch_simt_gemm(g, st));
     }
   }
-  // 4. dW1_e = dh_pre_e^T x_disp_e ; db1 = column sums of dh_pre
+  // 4. dW1_e = dh_pre_e^T x_disp_e ; db1 = column sums of dh_pre (bf16: the
+  //    data-gradient epilogue's partial sums, added here in a fixed order)
   bool db1_done = false;
+  if (dt == MOE_BF16) {
+    MOE_CUDA(launch_bias_grad_reduce(w.colpart, sv->expert_offsets, E, f, db1, st));
+    db1_done = true;
+  }
   if (dt == MOE_BF16) {
     TcWgrad g{};
     g.A = w.dh_pre; g.B = sv->x_disp; g.rows_alloc = R > 0 ? R : 1; g.C = dw1;
     g.M = f; g.N = d; g.G = E; g.offsets = sv->expert_offsets; g.err = device_error_ptr();
-    g.colsum = db1;
+    g.colsum = nullptr;
     // its own maps: the dW2 launch may still be reading the first half
     g.group_maps = w.maps ? static_cast<char *>(w.maps) + 2 * size_t(E) * kTensorMapBytes
                           : nullptr;
     cudaError_t e = launch_tc_wgrad(g, st);
-    db1_done = e == cudaSuccess;
+    db1_done = db1_done || (e == cudaSuccess && g.colsum != nullptr);
     if (e == cudaErrorNotSupported) {
       g.colsum = nullptr;
       e = launch_tc_wgrad(g, st);

@@ -167,6 +167,48 @@ combine_bwd_kernel(const uint4 *__restrict__ dy, const uint4 *__restrict__ out,
   }
 }
 
+// bf16 form: a CTA takes 64 columns of one group (a 128-byte segment of
+// each row), 8 threads across them (8 columns, 16 bytes each) and 32 row
+// groups down the group's rows (every 32nd row); the row groups are then
+// added in a fixed order.
+constexpr int kColsumCols = 64, kColsumRowGroups = 32;
+constexpr int kColsumThreads = (kColsumCols / 8) * kColsumRowGroups;
+
+__global__ void __launch_bounds__(kColsumThreads)
+group_colsum_bf16_kernel(const uint4 *__restrict__ M, int nvec,
+                         const int32_t *__restrict__ offsets, uint4 *__restrict__ db) {
+  griddep_begin();
+  __shared__ float part[kColsumRowGroups][kColsumCols + 1];
+  __shared__ float tot[kColsumCols];
+  const int g = blockIdx.y;
+  const int cv = threadIdx.x & 7, rg = threadIdx.x >> 3;
+  const int v = blockIdx.x * (kColsumCols / 8) + cv;  // this thread's 16-byte column vector
+  const int64_t r0 = offsets[g], r1 = offsets[g + 1];
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (v < nvec) {
+#pragma unroll 4
+    for (int64_t r = r0 + rg; r < r1; r += kColsumRowGroups) {
+      float x[8];
+      Vec<__nv_bfloat16>::to_f32(__ldcs(M + r * nvec + v), x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += x[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[rg][cv * 8 + i] = acc[i];
+  __syncthreads();
+  if (threadIdx.x < kColsumCols) {
+    float t = 0.0f;
+    for (int j = 0; j < kColsumRowGroups; ++j) t += part[j][threadIdx.x];
+    tot[threadIdx.x] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x < kColsumCols / 8) {
+    const int vo = blockIdx.x * (kColsumCols / 8) + threadIdx.x;
+    if (vo < nvec) db[int64_t(g) * nvec + vo] = Vec<__nv_bfloat16>::from_f32(&tot[threadIdx.x * 8]);
+  }
+}
+
 // db[g, n] = sum over rows of group g of M[r, n]; blockDim (32, 8)
 __global__ void group_colsum_kernel(const void *__restrict__ M, int dtype, int N,
                                     const int32_t *__restrict__ offsets,
@@ -374,6 +416,12 @@ cudaError_t launch_combine_bwd(const void *dy, const void *out_disp, int dtype, 
 
 cudaError_t launch_group_colsum(const void *M, int dtype, int N, int G,
                                 const int32_t *offsets, void *db, cudaStream_t st) {
+  if (dtype == MOE_BF16 && N % 8 == 0) {
+    dim3 grid((N + kColsumCols - 1) / kColsumCols, G);
+    return launch_k(group_colsum_bf16_kernel, grid, kColsumThreads, 0, st,
+                    static_cast<const uint4 *>(M), N / 8, offsets,
+                    static_cast<uint4 *>(db));
+  }
   dim3 grid((N + 31) / 32, G);
   return launch_k(group_colsum_kernel, grid, dim3(32, 8), 0, st, M, dtype, N, offsets, db);
 }

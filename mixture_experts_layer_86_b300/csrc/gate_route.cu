@@ -78,6 +78,7 @@ constexpr uint32_t kXBoxBytes = 128 * 128;      // 128 token rows x 64 bf16; TM 
 constexpr uint32_t kStgFloats = 32 * 33;        // one epilogue warp's transpose tile
 constexpr uint64_t kGrWaitNs = 2000000000ull;   // 2 s
 constexpr int kGrMaxBoxes = 4;                 // 64-wide K boxes per ring stage, at most
+constexpr int64_t kRehearseMinTile = 200 * 1024;  // tile elements (TM x d) that hide the rehearsal
 
 struct __align__(16) GrCtl {
   uint64_t full[kGrMaxStages];
@@ -118,6 +119,8 @@ struct GrParams {
   float *l_aux;
   int32_t *hist;        // [ntiles][hist_pitch] counts per (j, e)
   float *psum;          // [ntiles][psum_pitch] probability sums per e
+  int32_t *scratch;     // [kMaxExperts + 1]: where the last CTA's rehearsal of phase B writes
+  int rehearse;         // nonzero: the last CTA rehearses phase B before the grid barrier
   int hist_pitch, psum_pitch;
   int chunks_per_warp;  // 32-expert chunks each epilogue warp keeps in shared memory
   unsigned int *err;
@@ -177,6 +180,186 @@ __device__ __forceinline__ void issue_stage(const GrParams &p, const CUtensorMap
     const int k0 = (kb * p.nbox + b) * 64;
     ptx::tma_load_2d(ptx::smem_addr(st + b * kXBoxBytes), tmX, fb, k0, int32_t(tok0));
     ptx::tma_load_2d(ptx::smem_addr(st + p.nbox * kXBoxBytes + b * wbox_bytes), tmW, fb, k0, 0);
+  }
+}
+
+// Phase B of one CTA (see the header): the prefix of all tiles' counts, the
+// offsets, this tile's slots and row map; for the last CTA also the routed /
+// kept counts, the offsets and l_aux, written through `o`.  Not inlined: the
+// last CTA, which has no tile, runs it once with `o` pointing at scratch
+// before it joins the grid barrier, so that the code is in its instruction
+// cache when the real pass comes (each SM otherwise fetches this one-shot
+// code line by line from L2 or DRAM after the barrier).
+struct GrOut {
+  int32_t *routed, *kept, *offsets;
+  float *l_aux;
+};
+
+__device__ __noinline__ void gate_phase_b(const GrParams &p, GrCtl &ctl, uint8_t *ring, int tile,
+                                          bool okb, const GrOut o) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int64_t tok0 = int64_t(tile) * p.TM;
+  const int E = p.E, k = p.k;
+  // prefix and totals of the per-tile counts, 4 columns per load
+  {
+    const int nv = p.hist_pitch >> 2;
+    const int RG = max(1, kGrThreads / nv);
+    const int v = tid % nv, g = tid / nv;
+    int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+    const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
+    if (g < RG && okb) {
+      // 24 rows per round, every load issued before any is used: the prefix
+      // costs a round trip to L2 per 24 * RG tiles
+      constexpr int kU = 24;
+      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
+        int4 a[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int t = t0 + u * RG;
+          a[u] = t < p.ntiles ? __ldcg(h4 + int64_t(t) * nv + v) : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          tot = add4(tot, a[u]);
+          if (t0 + u * RG < tile) pre = add4(pre, a[u]);
+        }
+      }
+    }
+    int4 *red = reinterpret_cast<int4 *>(ring);  // [2][RG][nv]
+    if (g < RG) {
+      red[g * nv + v] = pre;
+      red[RG * nv + g * nv + v] = tot;
+    }
+    block_sync();
+    for (int i = tid; i < k * E; i += kGrThreads) {
+      const int vi = i >> 2, c = i & 3;
+      int P = 0, T = 0;
+      for (int gg = 0; gg < RG; ++gg) {
+        P += comp4(red[gg * nv + vi], c);
+        T += comp4(red[RG * nv + gg * nv + vi], c);
+      }
+      ctl.pre[i / E][i % E] = P;
+      ctl.tot[i / E][i % E] = T;
+    }
+    block_sync();
+  }
+  // routed / kept counts and the expert offsets (warp 0; lane l owns a
+  // contiguous range of experts)
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
+      local += (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFullMask, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
+      const int kp = (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
+      // offsets never pass the rows the buffers hold (true by construction
+      // when every tile's counts arrived)
+      ctl.offs[e] = run < p.rows_alloc ? run : int(p.rows_alloc);
+      if (tile == p.ntiles) {
+        o.routed[e] = rt;
+        o.kept[e] = kp;
+        o.offsets[e] = ctl.offs[e];
+      }
+      run += kp;
+    }
+    if (lane == 31) {
+      ctl.offs[E] = incl < p.rows_alloc ? incl : int(p.rows_alloc);
+      if (tile == p.ntiles) o.offsets[E] = ctl.offs[E];
+    }
+  }
+  block_sync();
+  // final slots and the row map of this tile's choices
+  for (int i = tid; i < p.TM * k; i += kGrThreads) {
+    const int r = i / k, j = i - r * k;
+    const int64_t s = tok0 + r;
+    if (s >= p.S) continue;
+    const int e = ctl.choice[j][r];
+    int pos = -1;
+    if (okb && e >= 0) {
+      pos = ctl.pre[j][e] + (j == 1 ? ctl.tot[0][e] : 0) + ctl.rank[j][r];
+      if (pos >= ctl.offs[e + 1] - ctl.offs[e]) pos = -1;  // beyond the capacity
+    }
+    p.slot[s * k + j] = pos;
+    if (pos >= 0) p.row_src[ctl.offs[e] + pos] = int32_t(s * k + j);
+  }
+  // l_aux (the last CTA): probability sums over all tiles, as exact fixed-point
+  if (tile == p.ntiles) {
+    const int nv = p.psum_pitch >> 2;
+    const int RG = max(1, kGrThreads / nv);
+    const int v = tid % nv, g = tid / nv;
+    long long a[4] = {0, 0, 0, 0};
+    const float4 *p4 = reinterpret_cast<const float4 *>(p.psum);
+    if (g < RG && okb) {
+      constexpr int kU = 16;
+      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
+        float4 f[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int t = t0 + u * RG;
+          f[u] = t < p.ntiles ? __ldcg(p4 + int64_t(t) * nv + v) : make_float4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          a[0] += fix30_tile(f[u].x);
+          a[1] += fix30_tile(f[u].y);
+          a[2] += fix30_tile(f[u].z);
+          a[3] += fix30_tile(f[u].w);
+        }
+      }
+    }
+    // the count reduction above is done with the ring: reuse it
+    long long *red = reinterpret_cast<long long *>(ring);  // [RG][psum_pitch]
+    if (g < RG)
+      for (int c = 0; c < 4; ++c) red[g * p.psum_pitch + v * 4 + c] = a[c];
+    block_sync();
+    for (int e = tid; e < E; e += kGrThreads) {
+      long long t = 0;
+      for (int gg = 0; gg < RG; ++gg) t += red[gg * p.psum_pitch + e];
+      ctl.aux[e] = t;
+    }
+    block_sync();
+    if (warp == 0) {
+      // fp32 from the exact integer sums (no FP64): lane l owns a
+      // contiguous range of experts, lanes are added in a fixed tree order
+      const int per = (E + 31) / 32;
+      const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+      const float S = float(p.S);
+      if (p.aux_type == MOE_AUX_STD) {
+        // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
+        long long sa = 0;
+        for (int e = e0; e < e1; ++e) sa += ctl.aux[e];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(kFullMask, sa, o);
+        float sq = 0.0f;
+        for (int e = e0; e < e1; ++e) {
+          const float dv = usage_deviation(ctl.aux[e], sa, E, p.S);
+          sq = fmaf(dv, dv, sq);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
+        if (lane == 0) *o.l_aux = okb ? sqrtf(sq / float(E)) + 1e-6f : NAN;
+      } else {
+        // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
+        float aux = 0.0f;
+        for (int e = e0; e < e1; ++e)
+          aux = fmaf(float(ctl.aux[e]) * kInvFix30, float(ctl.tot[0][e]), aux);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
+        if (lane == 0) *o.l_aux = okb ? float(E) * aux / S / S : NAN;
+      }
+    }
   }
 }
 
@@ -504,6 +687,14 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     }
   }
 
+  // the last CTA: phase B once on scratch outputs while the tiles stream
+  // (when their stream is long enough to hide it)
+  if (tile == p.ntiles && p.rehearse) {
+    const GrOut dry{p.scratch, p.scratch, p.scratch, reinterpret_cast<float *>(p.scratch)};
+    gate_phase_b(p, ctl, ring, tile, true, dry);
+    block_sync();
+  }
+
   // ------------------------------------------------------- grid barrier
   if (tid == 0) {
     const bool ok = grid_barrier(&g_gate_barrier[p.barrier_slot], unsigned(p.ntiles) + 1u, lim);
@@ -516,166 +707,7 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   const bool okb = ctl.barrier_ok != 0;
 
   // ------------------------------------------------------------ phase B
-  // prefix and totals of the per-tile counts, 4 columns per load
-  {
-    const int nv = p.hist_pitch >> 2;
-    const int RG = max(1, kGrThreads / nv);
-    const int v = tid % nv, g = tid / nv;
-    int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
-    const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
-    if (g < RG && okb) {
-      // 24 rows per round, every load issued before any is used: the prefix
-      // costs a round trip to L2 per 24 * RG tiles
-      constexpr int kU = 24;
-      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
-        int4 a[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int t = t0 + u * RG;
-          a[u] = t < p.ntiles ? __ldcg(h4 + int64_t(t) * nv + v) : make_int4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          tot = add4(tot, a[u]);
-          if (t0 + u * RG < tile) pre = add4(pre, a[u]);
-        }
-      }
-    }
-    int4 *red = reinterpret_cast<int4 *>(ring);  // [2][RG][nv]
-    if (g < RG) {
-      red[g * nv + v] = pre;
-      red[RG * nv + g * nv + v] = tot;
-    }
-    block_sync();
-    for (int i = tid; i < k * E; i += kGrThreads) {
-      const int vi = i >> 2, c = i & 3;
-      int P = 0, T = 0;
-      for (int gg = 0; gg < RG; ++gg) {
-        P += comp4(red[gg * nv + vi], c);
-        T += comp4(red[RG * nv + gg * nv + vi], c);
-      }
-      ctl.pre[i / E][i % E] = P;
-      ctl.tot[i / E][i % E] = T;
-    }
-    block_sync();
-  }
-  // routed / kept counts and the expert offsets (warp 0; lane l owns a
-  // contiguous range of experts)
-  if (warp == 0) {
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int local = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
-      local += (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(kFullMask, incl, o);
-      if (lane >= o) incl += t;
-    }
-    int run = incl - local;
-    for (int e = e0; e < e1; ++e) {
-      const int rt = ctl.tot[0][e] + (k == 2 ? ctl.tot[1][e] : 0);
-      const int kp = (p.cap < 0 || rt < p.cap) ? rt : int(p.cap);
-      // offsets never pass the rows the buffers hold (true by construction
-      // when every tile's counts arrived)
-      ctl.offs[e] = run < p.rows_alloc ? run : int(p.rows_alloc);
-      if (tile == p.ntiles) {
-        p.routed[e] = rt;
-        p.kept[e] = kp;
-        p.offsets[e] = ctl.offs[e];
-      }
-      run += kp;
-    }
-    if (lane == 31) {
-      ctl.offs[E] = incl < p.rows_alloc ? incl : int(p.rows_alloc);
-      if (tile == p.ntiles) p.offsets[E] = ctl.offs[E];
-    }
-  }
-  block_sync();
-  // final slots and the row map of this tile's choices
-  for (int i = tid; i < p.TM * k; i += kGrThreads) {
-    const int r = i / k, j = i - r * k;
-    const int64_t s = tok0 + r;
-    if (s >= p.S) continue;
-    const int e = ctl.choice[j][r];
-    int pos = -1;
-    if (okb && e >= 0) {
-      pos = ctl.pre[j][e] + (j == 1 ? ctl.tot[0][e] : 0) + ctl.rank[j][r];
-      if (pos >= ctl.offs[e + 1] - ctl.offs[e]) pos = -1;  // beyond the capacity
-    }
-    p.slot[s * k + j] = pos;
-    if (pos >= 0) p.row_src[ctl.offs[e] + pos] = int32_t(s * k + j);
-  }
-  // l_aux (the last CTA): probability sums over all tiles, as exact fixed-point
-  if (tile == p.ntiles) {
-    const int nv = p.psum_pitch >> 2;
-    const int RG = max(1, kGrThreads / nv);
-    const int v = tid % nv, g = tid / nv;
-    long long a[4] = {0, 0, 0, 0};
-    const float4 *p4 = reinterpret_cast<const float4 *>(p.psum);
-    if (g < RG && okb) {
-      constexpr int kU = 16;
-      for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
-        float4 f[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int t = t0 + u * RG;
-          f[u] = t < p.ntiles ? __ldcg(p4 + int64_t(t) * nv + v) : make_float4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          a[0] += fix30_tile(f[u].x);
-          a[1] += fix30_tile(f[u].y);
-          a[2] += fix30_tile(f[u].z);
-          a[3] += fix30_tile(f[u].w);
-        }
-      }
-    }
-    // the count reduction above is done with the ring: reuse it
-    long long *red = reinterpret_cast<long long *>(ring);  // [RG][psum_pitch]
-    if (g < RG)
-      for (int c = 0; c < 4; ++c) red[g * p.psum_pitch + v * 4 + c] = a[c];
-    block_sync();
-    for (int e = tid; e < E; e += kGrThreads) {
-      long long t = 0;
-      for (int gg = 0; gg < RG; ++gg) t += red[gg * p.psum_pitch + e];
-      ctl.aux[e] = t;
-    }
-    block_sync();
-    if (warp == 0) {
-      // fp32 from the exact integer sums (no FP64): lane l owns a
-      // contiguous range of experts, lanes are added in a fixed tree order
-      const int per = (E + 31) / 32;
-      const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-      const float S = float(p.S);
-      if (p.aux_type == MOE_AUX_STD) {
-        // l_aux = std_e(u_e) + 1e-6, u_e = sum_s p[s,e] / S (population std)
-        long long sa = 0;
-        for (int e = e0; e < e1; ++e) sa += ctl.aux[e];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(kFullMask, sa, o);
-        float sq = 0.0f;
-        for (int e = e0; e < e1; ++e) {
-          const float dv = usage_deviation(ctl.aux[e], sa, E, p.S);
-          sq = fmaf(dv, dv, sq);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(kFullMask, sq, o);
-        if (lane == 0) *p.l_aux = okb ? sqrtf(sq / float(E)) + 1e-6f : NAN;
-      } else {
-        // l_aux = E * sum_e (sum_s p[s,e] / S) * (first[e] / S)
-        float aux = 0.0f;
-        for (int e = e0; e < e1; ++e)
-          aux = fmaf(float(ctl.aux[e]) * kInvFix30, float(ctl.tot[0][e]), aux);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) aux += __shfl_xor_sync(kFullMask, aux, o);
-        if (lane == 0) *p.l_aux = okb ? float(E) * aux / S / S : NAN;
-      }
-    }
-  }
+  gate_phase_b(p, ctl, ring, tile, okb, GrOut{p.routed, p.kept, p.offsets, p.l_aux});
 }
 
 unsigned int next_barrier_slot() {
@@ -737,11 +769,18 @@ cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   if (ring < need) return cudaErrorNotSupported;
   const size_t smem = fixed + ring;
   if (smem > kSmemLimit) return cudaErrorNotSupported;
-  const size_t ws_need = size_t(p.ntiles) * (p.hist_pitch + p.psum_pitch) * 4;
+  const size_t ws_need =
+      size_t(p.ntiles) * (p.hist_pitch + p.psum_pitch) * 4 + (kMaxExperts + 4) * 4;
   if (ws_need > a.ws_bytes) return cudaErrorNotSupported;
   p.hist = static_cast<int32_t *>(a.ws);
   p.psum = reinterpret_cast<float *>(static_cast<char *>(a.ws) +
                                      size_t(p.ntiles) * p.hist_pitch * 4);
+  p.scratch = reinterpret_cast<int32_t *>(p.psum + size_t(p.ntiles) * p.psum_pitch);
+  // The rehearsal runs while the tiles stream x, with its instruction fetches
+  // competing for DRAM (~25 us); only tiles of at least ~230 k elements (the
+  // 64-expert layer's 112 x 2048) stream for that long, and with shorter
+  // tiles the last CTA would reach the grid barrier after them.
+  p.rehearse = int64_t(p.TM) * a.d >= kRehearseMinTile ? 1 : 0;
   p.idesc = ptx::idesc_bf16(128, p.E_pad, 0, 0);
   p.cap = a.cap;
   p.rows_alloc = a.rows_alloc;

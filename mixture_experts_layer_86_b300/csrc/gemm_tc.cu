@@ -448,7 +448,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
                     __nv_bfloat16 *__restrict__ C, __nv_bfloat16 *__restrict__ pre,
                     const __nv_bfloat16 *__restrict__ grad_src, int dact, unsigned int *err,
                     const __nv_bfloat16 *__restrict__ xg, const int32_t *__restrict__ row_src,
-                    int kch, int b_wrap, float *__restrict__ c_f32) {
+                    int kch, int b_wrap, float *__restrict__ c_f32,
+                    float *__restrict__ col_part) {
   griddep_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -711,6 +712,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
       const int64_t tok0 = int64_t(tc.row0) + int64_t(tc.tt) * kTok;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * kTok);
       const int nchunk = (tc.ntok + 31) >> 5;
+      float colacc = 0.0f;  // data-gradient form: this warp's sum over its tokens
 #pragma unroll 1
       for (int c = sub; c < nchunk; c += kSub) {
         uint32_t raw[32];
@@ -748,6 +750,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
             x[i] *= act_grad_fast(z, dact);
           }
           __syncwarp();
+          if (kWMN && col_part) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < ntk) colacc += x[i];
+          }
         }
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
@@ -770,6 +777,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmW,
           }
           __syncwarp();
         }
+      }
+      if (kWMN && col_part && f < N) {
+        // the bias gradient's partial of this token tile and warp: one slot
+        // per (token tile of the whole layer, warp class, feature)
+        const int tt_all = ctl.tile_start[tc.g] / nf + tc.tt;
+        col_part[(int64_t(tt_all) * kSub + sub) * N + f] = colacc;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -1564,6 +1577,33 @@ tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 }
 
+// db[g, n] = sum over the token tiles of group g (in order) and the warp
+// classes (in order) of the data-gradient epilogue's partials.
+__global__ void __launch_bounds__(256)
+bias_grad_reduce_kernel(const float *__restrict__ part, const int32_t *__restrict__ offsets,
+                        int N, int nsub, __nv_bfloat16 *__restrict__ db) {
+  griddep_begin();
+  __shared__ int s_base, s_cnt;
+  const int g = blockIdx.y;
+  if (threadIdx.x < 32) {  // the token tiles of the groups before g, a lane per group
+    int base = 0;
+    for (int j = threadIdx.x; j < g; j += 32) base += (offsets[j + 1] - offsets[j] + kTok - 1) / kTok;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) base += __shfl_xor_sync(kFullMask, base, o);
+    if (threadIdx.x == 0) {
+      s_base = base;
+      s_cnt = (offsets[g + 1] - offsets[g] + kTok - 1) / kTok;
+    }
+  }
+  __syncthreads();
+  const int n = blockIdx.x * 256 + threadIdx.x;
+  if (n >= N) return;
+  float acc = 0.0f;
+  for (int tt = s_base; tt < s_base + s_cnt; ++tt)
+    for (int sb = 0; sb < nsub; ++sb) acc += part[(int64_t(tt) * nsub + sb) * N + n];
+  db[int64_t(g) * N + n] = __float2bfloat16_rn(acc);
+}
+
 // ----------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1584,6 +1624,18 @@ EncodeTiledFn encode_fn() {
 }
 
 }  // namespace
+
+size_t bias_grad_part_bytes(int64_t max_rows, int G, int N) {
+  return size_t((max_rows + kTok - 1) / kTok + G) * (pair_epi_warps(false) / 4) * N * 4;
+}
+
+cudaError_t launch_bias_grad_reduce(const float *part, const int32_t *offsets, int G, int N,
+                                    void *db, cudaStream_t st) {
+  const dim3 grid(unsigned((N + 255) / 256), unsigned(G));
+  return launch_k(bias_grad_reduce_kernel, grid, 256, 0, st, part, offsets, N,
+                  pair_epi_warps(false) / 4, static_cast<__nv_bfloat16 *>(db));
+}
+
 
 bool make_bf16_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
                    uint32_t box_inner, uint32_t box_outer) {
@@ -1725,9 +1777,9 @@ cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st) {
                               static_cast<__nv_bfloat16 *>(g.pre),
                               static_cast<const __nv_bfloat16 *>(g.grad_src), g.dact, g.err,
                               static_cast<const __nv_bfloat16 *>(g.A), g.row_src, g.k_choices,
-                              g.b_wrap, g.c_f32);
+                              g.b_wrap, g.c_f32, g.col_part);
   }
-  if (g.row_src || g.b_wrap || g.c_f32)
+  if (g.row_src || g.b_wrap || g.c_f32 || g.col_part)
     return cudaErrorNotSupported;  // the gather and router forms need CTA pairs
   static PerDevice<int> smem_raised[2];
   const int which = g.b_kmajor ? 0 : 1;

@@ -206,7 +206,14 @@ struct TcGemm {
   int k_choices;
   int b_wrap, b_rows;      // router form: K rows of B repeat every b_wrap rows (0: off)
   float *c_f32;
+  // data-gradient form with grad_src (CTA pairs): the epilogue also writes
+  // partial column sums of its (fp32) output, bias_grad_part_bytes() of
+  // them, which launch_bias_grad_reduce adds into the bias gradient
+  float *col_part;
 };
+size_t bias_grad_part_bytes(int64_t max_rows, int G, int N);
+cudaError_t launch_bias_grad_reduce(const float *part, const int32_t *offsets, int G, int N,
+                                    void *db, cudaStream_t st);
 cudaError_t launch_tc_gemm(const TcGemm &g, cudaStream_t st);
 
 // K-grouped bf16 weight-gradient GEMM on the tensor cores:
