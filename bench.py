@@ -398,6 +398,44 @@ def stage_bytes(wl, R, with_probs=False):
             "combine": R * d * eb + S * d * eb + S * k * 12}
 
 
+def step_roofline(wl, R, peaks, ms_per_step):
+    """The step's floor: for every kernel of one step the larger of its
+    tensor time (its FLOP at the burst bf16 peak) and its memory time (its
+    algorithmic bytes at the measured copy bandwidth), summed.  Weights,
+    activations and bf16 tensors are read or written once; dW1 and dW2 are
+    written in fp32.  frac = floor / measured step time."""
+    S, d, f, E, k = wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k
+    eb = 2
+    P = (E + 63) // 64 * 64
+    train = wl.backward
+    byt = stage_bytes(wl, R, with_probs=train)
+    gemm = 2.0 * R * d * f
+    wb = E * d * f * eb  # one expert weight tensor (W1 or W2)
+    ks = [("gate", 0.0, byt["gate"]), ("dispatch", 0.0, byt["dispatch"]),
+          ("W1", gemm, wb + R * d * eb + (2 if train else 1) * R * f * eb),
+          ("W2", gemm, wb + R * f * eb + R * d * eb),
+          ("combine", 0.0, byt["combine"])]
+    if train:
+        ks += [("combine_bwd", 0.0, S * d * eb + 2 * R * d * eb + S * k * 4),
+               ("dW2", gemm, R * d * eb + R * f * eb + E * d * f * 4),
+               ("db2", 0.0, R * d * eb),
+               ("dh", gemm, wb + R * d * eb + 2 * R * f * eb),
+               ("dW1", gemm, R * f * eb + R * d * eb + E * f * d * 4),
+               ("dx_disp", gemm, wb + R * f * eb + R * d * eb),
+               ("router", 8.0 * S * d * P,
+                S * E * 4 + S * 2 * P * 2 + S * d * eb + E * d * 4 + 2 * S * d * 4
+                + R * d * eb + S * d * eb)]
+    kern = {}
+    for name, flops, nbytes in ks:
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        t_mem = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        kern[name] = {"us": round(max(t_tc, t_mem), 2), "bound": "tensor" if t_tc > t_mem else "hbm",
+                      "flop": flops, "bytes": nbytes}
+    floor_ms = sum(v["us"] for v in kern.values()) * 1e-3
+    return {"floor_ms": floor_ms, "frac": floor_ms / ms_per_step, "kernels": kern,
+            "peaks": "burst bf16 tensor, measured copy bandwidth"}
+
+
 def stage_breakdown(run, st, steps, peaks):
     """Per-stage times from a loop with an event at every stage boundary (a
     separate loop from the headline one, so its events do not perturb it)."""
@@ -623,6 +661,7 @@ def run_gpu(args):
                          "weights, 21x the 126 MB L2 (stages_cold_l2: gate, dispatch and "
                          "combine alone after a 512 MB flush)"},
         "roofline": roofline,
+        "step_roofline": step_roofline(wl, R, peaks, ms / args.steps),
         "stages": stages,
         "stages_cold_l2": cold,
         "e2e": {"value": job_tokens_per_s(world, S, args.steps, e2e_ms), "unit": "tokens/s",
@@ -672,6 +711,8 @@ def config_line(wl, args, dev, st, peaks, max_over_ranks, world, barrier, with_c
     if wl.backward:
         bwd_flops = 8.0 * R * wl.hidden_size * wl.ffn_size
         out["backward_TFLOP/s"] = bwd_flops / (stages["backward"]["ms"] * 1e-3) / 1e12
+    if wl.dtype == "bf16":
+        out["step_roofline"] = step_roofline(wl, R, peaks, ms / args.steps)
     if with_cpu:
         out["cpu_baseline"] = cpu_baseline(wl, run.inp_cpu, run.bufs["topk_idx"].cpu().numpy())
     del run
