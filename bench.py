@@ -388,6 +388,40 @@ def timed(torch, st, steps, body, barrier=None):
     return e0.elapsed_time(e1)
 
 
+def host_link(torch, dev, x_host, y_host, reps=10):
+    """Copy bandwidth of the host link for the end-to-end leg's own pinned
+    buffers: host-to-device alone, device-to-host alone, and both at once on
+    two streams (the pipeline's steady state), in GB/s per direction."""
+    xd, yd = torch.empty_like(x_host, device=dev), torch.empty_like(y_host, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nbytes = x_host.numel() * x_host.element_size()
+
+    def run(h2d, d2h):
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(s_in)
+        ev[2].record(s_out)
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    xd.copy_(x_host, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    y_host.copy_(yd, non_blocking=True)
+        ev[1].record(s_in)
+        ev[3].record(s_out)
+        torch.cuda.synchronize()
+        return max(ev[0].elapsed_time(ev[1]) if h2d else 0.0,
+                   ev[2].elapsed_time(ev[3]) if d2h else 0.0) / reps
+
+    run(True, True)
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    del xd, yd
+    gbs = lambda ms: nbytes / (ms * 1e-3) / 1e9
+    return {"bytes": nbytes, "h2d_gbs": gbs(t_in), "d2h_gbs": gbs(t_out),
+            "both_gbs_per_direction": gbs(t_both), "both_ms": t_both}
+
+
 def stage_bytes(wl, R, with_probs=False):
     """Algorithmic HBM bytes of the gate, dispatch and combine stages: each
     input read once, each output written once."""
@@ -598,6 +632,7 @@ def run_gpu(args):
     # the last step's result really is on the host
     assert torch.equal(y_host[(args.steps - 1) % 2], run.y.cpu()), "e2e result differs"
     del pipe
+    link = host_link(torch, dev, x_host[0], y_host[0])
 
     decode = decode_step(args, dev, max_over_ranks, world, peaks)
     residual = residual_step(args, dev, run, max_over_ranks, world)
@@ -669,7 +704,12 @@ def run_gpu(args):
                 "d2h_bytes_per_step": S * dm * eb + 4 * (1 + E),
                 "ms_per_step": e2e_ms / args.steps,
                 "timing": "CUDA events: before the first host-to-device copy, after the last "
-                          "device-to-host copy"},
+                          "device-to-host copy",
+                "host_link": link,
+                # steady state of the pipeline: the slower of the forward and the
+                # two copies running at once
+                "floor_ms": max(ms / args.steps, link["both_ms"]),
+                "frac_of_floor": max(ms / args.steps, link["both_ms"]) / (e2e_ms / args.steps)},
         "moe_forward_ms_per_step": fwd_call_ms / args.steps,
         "moe_forward_fused_dispatch_ms_per_step": fused_ms / args.steps,
         "dispatch": "fused into the first expert GEMM" if run_fused else "copy kernel",

@@ -64,55 +64,77 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
 #pragma unroll
   for (int q = 0; q < kMaxPerLane; ++q) pacc[q] = 0.0f;
 
-  // ---- phase 1: one warp per token, lanes over experts
-  for (int t = warp; t < kTB; t += kWarps) {
-    if (tok0 + t >= S) {
-      if (lane == 0) {
-        s_choice[0][t] = -1;
-        s_choice[1][t] = -1;
-      }
+  // ---- phase 1: a segment of W lanes per token (W = E rounded up to a power
+  // of two, at most 32), lanes over experts; a warp takes 32 / W tokens per
+  // pass, so small expert counts do not leave a warp's tokens in one long
+  // dependent chain.  Every reduction gives the full-warp result bit for bit.
+  const int W = E > 16 ? 32 : E > 8 ? 16 : E > 4 ? 8 : E > 2 ? 4 : E > 1 ? 2 : 1;
+  const int tpp = 32 / W;
+  const int sub = lane / W, sl = lane % W;
+  // each iteration loads the token rows (logits) of the next pass, then
+  // works on the current one (the first iteration only loads)
+  const int step = kWarps * tpp;
+  float vn[kMaxPerLane], v[kMaxPerLane];
+  int64_t s_cur = -1;
+  for (int t0 = warp * tpp - step; t0 < kTB; t0 += step) {
+    int64_t s_nx = -1;
+    if (t0 + step < kTB) {
+      s_nx = tok0 + t0 + step + sub;
+      if (s_nx >= S) s_nx = -1;
+      else if (noise.rts) s_nx = int64_t(rng::token_at(perm, uint32_t(s_nx)));
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) {
+      const int e = sl + 32 * q;
+      vn[q] = (s_nx >= 0 && q < nq && e < E) ? __ldg(logits + s_nx * E + e) : -INFINITY;
+    }
+    if (t0 < 0) {
+#pragma unroll
+      for (int q = 0; q < kMaxPerLane; ++q) v[q] = vn[q];
+      s_cur = s_nx;
       continue;
     }
-    const int64_t s = noise.rts ? int64_t(rng::token_at(perm, uint32_t(tok0 + t))) : tok0 + t;
-    const float *row = logits + s * E;
-    float v[kMaxPerLane], key_v[kMaxPerLane];
+    const int t = t0 + sub;
+    const bool live = s_cur >= 0;
+    const int64_t s = live ? s_cur : 0;
+    float key_v[kMaxPerLane];
     float m = -INFINITY;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      const int e = lane + 32 * q;
-      v[q] = (q < nq && e < E) ? row[e] : -INFINITY;
+      const int e = sl + 32 * q;
+      const bool has = live && q < nq && e < E;
       m = fmaxf(m, v[q]);
       key_v[q] = v[q];
-      if (use_gumbel && q < nq && e < E) {
+      if (use_gumbel && has) {
         // the selection key: logit + Gumbel noise, one float32 addition
         const uint4 w4 = rng::block(key, rng::kPurposeGateNoise, uint32_t(s), uint32_t(e >> 2));
         key_v[q] = __fadd_rn(v[q], rng::gumbel(rng::uniform(rng::word(w4, e & 3))));
       }
     }
-    m = warp_max(m);
+    m = seg_max(m, W);
     float ex[kMaxPerLane];
     float z = 0.0f;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      const int e = lane + 32 * q;
-      ex[q] = (q < nq && e < E) ? expf((v[q] - m) * inv_temp) : 0.0f;
+      const int e = sl + 32 * q;
+      ex[q] = (live && q < nq && e < E) ? expf((v[q] - m) * inv_temp) : 0.0f;
       z += ex[q];
     }
-    z = warp_sum(z);
+    z = seg_sum(z, W);
     const float inv_z = 1.0f / z;
     // top-1 (ties -> lower index), on the noisy keys under rsample
     float b1 = -INFINITY;
     int i1 = -1;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      const int e = lane + 32 * q;
+      const int e = sl + 32 * q;
       const float c = sample_all ? key_v[q] : v[q];
-      if (q < nq && e < E && (i1 < 0 || c > b1)) {
+      if (live && q < nq && e < E && (i1 < 0 || c > b1)) {
         b1 = c;
         i1 = e;
       }
     }
-    warp_argmax(b1, i1);
+    seg_argmax(b1, i1, W);
     int i2 = -1;
     if (k == 2) {
       // the second choice: on the noisy keys under rsample or second-choice
@@ -120,54 +142,67 @@ route_topk_kernel(const float *__restrict__ logits, int64_t S, int E, int k, flo
       float b2 = -INFINITY;
 #pragma unroll
       for (int q = 0; q < kMaxPerLane; ++q) {
-        const int e = lane + 32 * q;
+        const int e = sl + 32 * q;
         const float c = use_gumbel ? key_v[q] : v[q];
-        if (q < nq && e < E && e != i1 && (i2 < 0 || c > b2)) {
+        if (live && q < nq && e < E && e != i1 && (i2 < 0 || c > b2)) {
           b2 = c;
           i2 = e;
         }
       }
-      warp_argmax(b2, i2);
+      seg_argmax(b2, i2, W);
     }
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      const int e = lane + 32 * q;
-      if (q < nq && e < E) {
+      const int e = sl + 32 * q;
+      if (live && q < nq && e < E) {
         const float p = ex[q] * inv_z;
         pacc[q] += p;
         if (probs) probs[s * E + e] = p;
       }
     }
-    // exp(l - max) of the chosen experts, broadcast from the lanes holding them
+    // exp(l - max) of the chosen experts, from the segment lanes holding them
     float x1 = 0.0f, x2 = 0.0f;
 #pragma unroll
     for (int q = 0; q < kMaxPerLane; ++q) {
-      const float a = __shfl_sync(kFullMask, ex[q], i1 & 31);
-      if ((i1 >> 5) == q) x1 = a;
+      const float a = __shfl_sync(kFullMask, ex[q], i1 & 31, W);
+      if (i1 >= 0 && (i1 >> 5) == q) x1 = a;
       if (k == 2) {
-        const float b = __shfl_sync(kFullMask, ex[q], i2 & 31);
-        if ((i2 >> 5) == q) x2 = b;
+        const float b = __shfl_sync(kFullMask, ex[q], i2 & 31, W);
+        if (i2 >= 0 && (i2 >> 5) == q) x2 = b;
       }
     }
-    if (lane == 0) {
-      s_choice[0][t] = i1;
-      idx_out[s * k] = i1;
-      if (k == 1) {
-        w_out[s] = x1 * inv_z;
+    if (sl == 0) {
+      if (!live) {
+        s_choice[0][t] = -1;
         s_choice[1][t] = -1;
       } else {
-        const float den = x1 + x2;
-        w_out[s * 2] = x1 / den;
-        w_out[s * 2 + 1] = x2 / den;
-        idx_out[s * 2 + 1] = i2;
-        s_choice[1][t] = i2;
+        s_choice[0][t] = i1;
+        idx_out[s * k] = i1;
+        if (k == 1) {
+          w_out[s] = x1 * inv_z;
+          s_choice[1][t] = -1;
+        } else {
+          const float den = x1 + x2;
+          w_out[s * 2] = x1 / den;
+          w_out[s * 2 + 1] = x2 / den;
+          idx_out[s * 2 + 1] = i2;
+          s_choice[1][t] = i2;
+        }
       }
     }
+#pragma unroll
+    for (int q = 0; q < kMaxPerLane; ++q) v[q] = vn[q];
+    s_cur = s_nx;
   }
+  // the segments of a warp hold partial sums of the same experts: add them
+  // (lanes of equal sl, in a fixed order)
+#pragma unroll
+  for (int q = 0; q < kMaxPerLane; ++q)
+    for (int o = W; o < 32; o <<= 1) pacc[q] += __shfl_xor_sync(kFullMask, pacc[q], o);
 #pragma unroll
   for (int q = 0; q < kMaxPerLane; ++q) {
-    const int e = lane + 32 * q;
-    if (q < nq && e < E) s_psum[warp][e] = pacc[q];
+    const int e = sl + 32 * q;
+    if (sub == 0 && q < nq && e < E) s_psum[warp][e] = pacc[q];
   }
   block_sync();
   for (int e = threadIdx.x; e < E; e += kTB) {
