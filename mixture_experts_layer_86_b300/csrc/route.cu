@@ -38,6 +38,30 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Reductions within aligned segments of w lanes (w a power of two <= 32; all
+// 32 lanes call them).  Over the lanes that hold values, with the others at
+// the neutral element, each gives the full-warp tree's result bit for bit:
+// the tree only drops additions of zero (maxima of -inf).
+__device__ __forceinline__ float seg_sum(float v, int w) {
+  for (int o = w >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+__device__ __forceinline__ float seg_max(float v, int w) {
+  for (int o = w >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  return v;
+}
+__device__ __forceinline__ void seg_argmax(float &v, int &idx, int w) {
+  for (int o = w >> 1; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(kFullMask, v, o);
+    const int oi = __shfl_xor_sync(kFullMask, idx, o);
+    const bool take = (oi >= 0) && (idx < 0 || ov > v || (ov == v && oi < idx));
+    if (take) {
+      v = ov;
+      idx = oi;
+    }
+  }
+}
+
 // Under random token selection (noise.rts) CTA b works on the tokens at
 // queue positions b*kTB ... b*kTB + kTB - 1 instead of those token indices,
 // so counts and ranks come out in queue order; every per-token output is
