@@ -209,9 +209,12 @@ __device__ __noinline__ void gate_phase_b(const GrParams &p, GrCtl &ctl, uint8_t
     int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
     const int4 *h4 = reinterpret_cast<const int4 *>(p.hist);
     if (g < RG && okb) {
-      // 24 rows per round, every load issued before any is used: the prefix
-      // costs a round trip to L2 per 24 * RG tiles
-      constexpr int kU = 24;
+      // 8 rows per round, every load issued before any is used: the prefix
+      // costs a round trip to L2 per 8 * RG tiles.  Wider rounds are faster
+      // with the code cached, but this code runs once per launch and is
+      // fetched cold inside a step: 24 rows per round (and 16 for the
+      // probability sums below) made the launch 3-6 us slower there.
+      constexpr int kU = 8;
       for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
         int4 a[kU];
 #pragma unroll
@@ -302,7 +305,7 @@ __device__ __noinline__ void gate_phase_b(const GrParams &p, GrCtl &ctl, uint8_t
     long long a[4] = {0, 0, 0, 0};
     const float4 *p4 = reinterpret_cast<const float4 *>(p.psum);
     if (g < RG && okb) {
-      constexpr int kU = 16;
+      constexpr int kU = 4;
       for (int t0 = g; t0 < p.ntiles; t0 += kU * RG) {
         float4 f[kU];
 #pragma unroll
@@ -576,12 +579,15 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         }
       }
       const float m = b1;  // the top-1 logit is the softmax shift
-      // pass 2: exp((l - m) / T) in place; this half's sum
+      // pass 2: exp((l - m) / T) in place; this half's sum.  Passes 2 and 3
+      // work on shared memory and are only partly unrolled: the epilogue
+      // runs once per launch and is fetched cold inside a step, where the
+      // smaller code made the launch ~2 us faster
       float z = 0.0f;
       for (int ci = 0; ci < my_chunks; ++ci) {
         const int c = h + 2 * ci;
         float *stg = stg0 + ci * kStgFloats;
-  #pragma unroll
+  #pragma unroll 4
         for (int t = 0; t < 32; ++t) {
           if (c * 32 + t < E) {
             const float ev = expf((stg[lane * 33 + t] - m) * p.inv_temp);
@@ -598,13 +604,13 @@ gate_route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
       for (int ci = 0; ci < my_chunks; ++ci) {
         const int c = h + 2 * ci;
         float *stg = stg0 + ci * kStgFloats;
-  #pragma unroll
+  #pragma unroll 8
         for (int t = 0; t < 32; ++t)
           if (c * 32 + t < E) stg[lane * 33 + t] = valid ? stg[lane * 33 + t] * inv_z : 0.0f;
         __syncwarp();
         const int e = c * 32 + lane;
         float cs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows rr = 4 i + u, fixed order
-  #pragma unroll
+  #pragma unroll 2
         for (int rr = 0; rr < 32; rr += 4) {
   #pragma unroll
           for (int u = 0; u < 4; ++u) cs[u] += stg[(rr + u) * 33 + lane];
