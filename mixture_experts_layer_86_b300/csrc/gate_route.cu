@@ -78,7 +78,10 @@ constexpr uint32_t kXBoxBytes = 128 * 128;      // 128 token rows x 64 bf16; TM 
 constexpr uint32_t kStgFloats = 32 * 33;        // one epilogue warp's transpose tile
 constexpr uint64_t kGrWaitNs = 2000000000ull;   // 2 s
 constexpr int kGrMaxBoxes = 4;                 // 64-wide K boxes per ring stage, at most
-constexpr int64_t kRehearseMinTile = 200 * 1024;  // tile elements (TM x d) that hide the rehearsal
+// tile elements (TM x d) from which the rehearsal pays: inside a step it
+// made the gate 4 us faster at 56 x 1024 (and is needed at 112 x 2048), 4 us
+// slower at 32 x 512, where the tiles finish before it does
+constexpr int64_t kRehearseMinTile = 32 * 1024;
 
 struct __align__(16) GrCtl {
   uint64_t full[kGrMaxStages];
@@ -782,10 +785,9 @@ cudaError_t launch_gate_route(const GateRouteArgs &a, cudaStream_t st) {
   p.psum = reinterpret_cast<float *>(static_cast<char *>(a.ws) +
                                      size_t(p.ntiles) * p.hist_pitch * 4);
   p.scratch = reinterpret_cast<int32_t *>(p.psum + size_t(p.ntiles) * p.psum_pitch);
-  // The rehearsal runs while the tiles stream x, with its instruction fetches
-  // competing for DRAM (~25 us); only tiles of at least ~230 k elements (the
-  // 64-expert layer's 112 x 2048) stream for that long, and with shorter
-  // tiles the last CTA would reach the grid barrier after them.
+  // The rehearsal runs while the tiles stream x and run their epilogue; with
+  // tiles much smaller than kRehearseMinTile the last CTA would reach the
+  // grid barrier after them.
   p.rehearse = int64_t(p.TM) * a.d >= kRehearseMinTile ? 1 : 0;
   p.idesc = ptx::idesc_bf16(128, p.E_pad, 0, 0);
   p.cap = a.cap;
