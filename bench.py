@@ -436,11 +436,10 @@ def step_roofline(wl, R, peaks, ms_per_step):
     """The step's floor: for every kernel of one step the larger of its
     tensor time (its FLOP at the burst bf16 peak) and its memory time (its
     algorithmic bytes at the measured copy bandwidth), summed.  Weights,
-    activations and bf16 tensors are read or written once; dW1 and dW2 are
-    written in fp32.  frac = floor / measured step time."""
+    activations and gradients are bf16, each read or written once.
+    frac = floor / measured step time."""
     S, d, f, E, k = wl.num_tokens, wl.hidden_size, wl.ffn_size, wl.num_experts, wl.k
     eb = 2
-    P = (E + 63) // 64 * 64
     train = wl.backward
     byt = stage_bytes(wl, R, with_probs=train)
     gemm = 2.0 * R * d * f
@@ -451,14 +450,15 @@ def step_roofline(wl, R, peaks, ms_per_step):
           ("combine", 0.0, byt["combine"])]
     if train:
         ks += [("combine_bwd", 0.0, S * d * eb + 2 * R * d * eb + S * k * 4),
-               ("dW2", gemm, R * d * eb + R * f * eb + E * d * f * 4),
+               ("dW2", gemm, R * d * eb + R * f * eb + wb),
                ("db2", 0.0, R * d * eb),
                ("dh", gemm, wb + R * d * eb + 2 * R * f * eb),
-               ("dW1", gemm, R * f * eb + R * d * eb + E * f * d * 4),
+               ("dW1", gemm, R * f * eb + R * d * eb + wb),
                ("dx_disp", gemm, wb + R * f * eb + R * d * eb),
-               ("router", 8.0 * S * d * P,
-                S * E * 4 + S * 2 * P * 2 + S * d * eb + E * d * 4 + 2 * S * d * 4
-                + R * d * eb + S * d * eb)]
+               # router backward: probs in, dW_g = dlogitsT x, and
+               # dX = dlogits W_g + the gathered dx_disp rows
+               ("router", 4.0 * S * d * E,
+                S * E * 4 + S * d * eb + E * d * eb + R * d * eb + S * d * eb)]
     kern = {}
     for name, flops, nbytes in ks:
         t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
